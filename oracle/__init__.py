@@ -1,0 +1,248 @@
+"""CPU oracle for the MoE expert-parallel routing plan, dispatch and combine.
+
+TEST INFRASTRUCTURE ONLY.  Only the test-suite, the smoke check and the CPU
+baseline leg of the benchmark may import this package.  The product library
+(``combine_ep_plan_gb300``) never imports it and shares no code with it.
+
+The arithmetic lives in ``ep_oracle.c`` (plain C, compiled with gcc, no
+fast-math, no FP contraction).  This module only compiles it on demand,
+allocates numpy outputs and calls it through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import tempfile
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ep_oracle.c")
+_LIB = os.path.join(_HERE, "libep_oracle.so")
+
+OK = 0
+ERR_INVALID = 1
+ERR_CAPACITY = 2
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int):
+        super().__init__({ERR_INVALID: "invalid routing input",
+                          ERR_CAPACITY: "output capacity too small"}.get(code, f"error {code}"))
+        self.code = code
+
+
+def build(force: bool = False) -> str:
+    """Compile ep_oracle.c into libep_oracle.so next to it (atomic rename)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    os.close(fd)
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    try:
+        subprocess.run(cmd, check=True, capture_output=True, text=True)
+        os.replace(tmp, _LIB)
+    except subprocess.CalledProcessError as exc:  # pragma: no cover
+        os.unlink(tmp)
+        raise RuntimeError(f"oracle build failed:\n{exc.stderr}") from exc
+    return _LIB
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        i32 = ctypes.c_int
+        lib.ep_oracle_validate.argtypes = [P, i64, i32, i32, i32, i32, i32]
+        lib.ep_oracle_validate.restype = i32
+        lib.ep_oracle_plan.argtypes = [P, i64, i32, i32, i32, i32, i32] + [P] * 11 + [i64, P, P, P, i64, P]
+        lib.ep_oracle_plan.restype = i32
+        lib.ep_oracle_dispatch_bf16.argtypes = [P, i64, P, i64, i32, P]
+        lib.ep_oracle_dispatch_bf16.restype = None
+        lib.ep_oracle_dispatch_fp8.argtypes = [P, i64, P, i64, i32, P, P]
+        lib.ep_oracle_dispatch_fp8.restype = None
+        lib.ep_oracle_combine.argtypes = [P, i64, P, P, i64, i32, P]
+        lib.ep_oracle_combine.restype = None
+        lib.ep_oracle_expert_scale.argtypes = [P, i64, P, P, i32, P]
+        lib.ep_oracle_expert_scale.restype = None
+        lib.ep_oracle_expert_dequant.argtypes = [P, P, i64, i64, P]
+        lib.ep_oracle_expert_dequant.restype = None
+        lib.ep_oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+        lib.ep_oracle_f32_to_bf16.restype = ctypes.c_uint16
+        lib.ep_oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+        lib.ep_oracle_bf16_to_f32.restype = ctypes.c_float
+        lib.ep_oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+        lib.ep_oracle_f32_to_e4m3.restype = ctypes.c_uint8
+        lib.ep_oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+        lib.ep_oracle_e4m3_to_f32.restype = ctypes.c_float
+        lib.ep_oracle_max_recv_rows.argtypes = [i64, i32, i32]
+        lib.ep_oracle_max_recv_rows.restype = i64
+        lib.ep_oracle_max_expanded_rows.argtypes = [i64, i32, i32, i32, i32]
+        lib.ep_oracle_max_expanded_rows.restype = i64
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+@dataclass
+class Plan:
+    """All plan outputs, named as in the dispatch handle of the pages."""
+    S: int
+    P: int
+    K: int
+    E: int
+    A: int
+    C: int
+    is_token_in_rank: np.ndarray      # [T,P] u8
+    num_tokens_per_rank: np.ndarray   # [P,P] i32  [s][d]
+    num_tokens_per_expert: np.ndarray  # [P,E] i32  [s][e]
+    expert_counts: np.ndarray         # [E]   i32
+    num_recv: np.ndarray              # [P]   i32
+    rank_prefix: np.ndarray           # [P,P] i32  inclusive over sources
+    channel_prefix: np.ndarray        # [P,P,C] i32 [s][d][c] inclusive over channels
+    recv_channel_prefix: np.ndarray   # [P,P,C] i32 [d][s][c] segment start
+    send_head: np.ndarray             # [T,P] i32
+    recv_offsets: np.ndarray          # [P+1] i32
+    recv_src_idx: np.ndarray          # [N_recv] i32
+    expert_offsets: np.ndarray        # [E+1] i32
+    slot: np.ndarray                  # [T,K] i32
+    exp_src: np.ndarray               # [N_exp] i32
+
+    @property
+    def T(self) -> int:
+        return self.P * self.S
+
+    @property
+    def num_expanded(self) -> int:
+        return int(self.expert_offsets[-1])
+
+    @property
+    def num_recv_total(self) -> int:
+        return int(self.recv_offsets[-1])
+
+
+def default_channels(S: int, C: int = 0) -> int:
+    return C if C > 0 else max(1, min(16, S))
+
+
+def validate(topk_idx: np.ndarray, S: int, P: int, E: int, A: int, C: int = 0) -> int:
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    K = idx.shape[1]
+    return _load().ep_oracle_validate(_ptr(idx), S, P, K, E, A, default_channels(S, C))
+
+
+def plan(topk_idx: np.ndarray, S: int, P: int, E: int, A: int, C: int = 0) -> Plan:
+    lib = _load()
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int64)
+    T, K = idx.shape
+    assert T == P * S, "topk_idx must have P*S rows"
+    C = default_channels(S, C)
+    rcap = max(1, lib.ep_oracle_max_recv_rows(S, P, K))
+    xcap = max(1, lib.ep_oracle_max_expanded_rows(S, P, K, E, A))
+    o = dict(
+        is_token_in_rank=np.zeros((T, P), np.uint8),
+        num_tokens_per_rank=np.zeros((P, P), np.int32),
+        num_tokens_per_expert=np.zeros((P, E), np.int32),
+        expert_counts=np.zeros(E, np.int32),
+        num_recv=np.zeros(P, np.int32),
+        rank_prefix=np.zeros((P, P), np.int32),
+        channel_prefix=np.zeros((P, P, C), np.int32),
+        recv_channel_prefix=np.zeros((P, P, C), np.int32),
+        send_head=np.zeros((T, P), np.int32),
+        recv_offsets=np.zeros(P + 1, np.int32),
+        recv_src_idx=np.zeros(rcap, np.int32),
+        expert_offsets=np.zeros(E + 1, np.int32),
+        slot=np.zeros((T, K), np.int32),
+        exp_src=np.zeros(xcap, np.int32),
+    )
+    sizes = np.zeros(2, np.int64)
+    rc = lib.ep_oracle_plan(
+        _ptr(idx), S, P, K, E, A, C,
+        _ptr(o["is_token_in_rank"]), _ptr(o["num_tokens_per_rank"]),
+        _ptr(o["num_tokens_per_expert"]), _ptr(o["expert_counts"]), _ptr(o["num_recv"]),
+        _ptr(o["rank_prefix"]), _ptr(o["channel_prefix"]), _ptr(o["recv_channel_prefix"]),
+        _ptr(o["send_head"]), _ptr(o["recv_offsets"]), _ptr(o["recv_src_idx"]), rcap,
+        _ptr(o["expert_offsets"]), _ptr(o["slot"]), _ptr(o["exp_src"]), xcap, _ptr(sizes))
+    if rc != OK:
+        raise OracleError(rc)
+    o["recv_src_idx"] = o["recv_src_idx"][: int(sizes[0])].copy()
+    o["exp_src"] = o["exp_src"][: int(sizes[1])].copy()
+    return Plan(S=S, P=P, K=K, E=E, A=A, C=C, **o)
+
+
+def dispatch_bf16(x_bits: np.ndarray, pl: Plan, zero_pad: bool = True) -> np.ndarray:
+    """x_bits: [T,H] uint16 bf16 bit patterns -> [N_exp,H] uint16."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    H = x.shape[1]
+    n = pl.num_expanded
+    out = np.zeros((n, H), np.uint16)
+    _load().ep_oracle_dispatch_bf16(_ptr(x), H, _ptr(pl.exp_src), n, int(zero_pad), _ptr(out))
+    return out
+
+
+def dispatch_fp8(x_bits: np.ndarray, pl: Plan, zero_pad: bool = True):
+    """-> (q [N_exp,H] uint8 E4M3 codes, scales [N_exp,H/128] float32)."""
+    x = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    H = x.shape[1]
+    assert H % 128 == 0
+    n = pl.num_expanded
+    q = np.zeros((n, H), np.uint8)
+    sc = np.zeros((n, H // 128), np.float32)
+    _load().ep_oracle_dispatch_fp8(_ptr(x), H, _ptr(pl.exp_src), n, int(zero_pad), _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def combine(y_bits: np.ndarray, pl: Plan, topk_weights: np.ndarray) -> np.ndarray:
+    """y_bits: [N_exp,H] uint16 bf16; topk_weights [T,K] f32 -> [T,H] uint16 bf16."""
+    y = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    H = y.shape[1]
+    out = np.zeros((pl.T, H), np.uint16)
+    _load().ep_oracle_combine(_ptr(y), H, _ptr(pl.slot), _ptr(w), pl.T, pl.K, _ptr(out))
+    return out
+
+
+def expert_scale(x_exp_bits: np.ndarray, pl: Plan) -> np.ndarray:
+    x = np.ascontiguousarray(x_exp_bits, dtype=np.uint16)
+    H = x.shape[1]
+    y = np.zeros_like(x)
+    _load().ep_oracle_expert_scale(_ptr(x), H, _ptr(pl.exp_src), _ptr(pl.expert_offsets), pl.E, _ptr(y))
+    return y
+
+
+def expert_dequant(q: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    sc = np.ascontiguousarray(scales, dtype=np.float32)
+    n, H = q.shape
+    y = np.zeros((n, H), np.uint16)
+    _load().ep_oracle_expert_dequant(_ptr(q), _ptr(sc), H, n, _ptr(y))
+    return y
+
+
+def f32_to_bf16(v: float) -> int:
+    return int(_load().ep_oracle_f32_to_bf16(v))
+
+
+def bf16_to_f32(b: int) -> float:
+    return float(_load().ep_oracle_bf16_to_f32(b))
+
+
+def f32_to_e4m3(v: float) -> int:
+    return int(_load().ep_oracle_f32_to_e4m3(v))
+
+
+def e4m3_to_f32(b: int) -> float:
+    return float(_load().ep_oracle_e4m3_to_f32(b))
