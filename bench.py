@@ -1,0 +1,472 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE expert-parallel hot path on GB300.
+
+One step = one pass of the whole hot path on one batch of synthetic routing:
+fresh routing plan -> BF16 dispatch (row scatter, zero padding) -> combine
+(identity expert: the dispatched rows are the expert outputs), on the
+workload P=8 ranks, E=64 experts, S=2048 tokens/rank (T=16384), hidden 7168,
+top-6, expert_alignment 128.
+
+Prints ONE JSON line (rank 0).  `value` is the HBM-ledger throughput of the
+whole step in GB/s (bytes the method must move: routing plan + dispatch +
+combine, see `ledger`) over device time with inputs resident in HBM; the same
+line carries tokens/s, the roofline of the dominant kernel, the end-to-end
+number through the C ABI with host buffers, the CPU oracle baseline and the
+SM clocks seen during the timed region.
+
+`--impl reference` times the CPU oracle (the reference arm) instead.
+With --gpus N > 1 (torchrun, one rank per GPU) every rank runs an
+independent replica: the path does not shard across GPUs.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "dispatch+combine GB/s and tokens/s on 1×GB300; % of HBM roofline"
+FALLBACK_HBM_GBS = 6800.0
+KERNELS_PER_STEP = 5  # count, emit, prefix (plan) + dispatch + combine
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only: barrier and max over ranks)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(use_cuda: bool):
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("nccl" if use_cuda else "gloo")
+    return rank, world, local
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float) -> float:
+    """Max of a host float over all ranks (identity when not distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_bytes: float, per_rank_tokens: float, local_ms: float, world: int, steps: int):
+    """Whole-job throughput: units of all ranks over the slowest rank's time."""
+    t_ms = max_over_ranks(local_ms)
+    per_step_s = t_ms / 1e3 / steps
+    return {
+        "ms_per_step": t_ms / steps,
+        "gbs": world * per_rank_bytes / per_step_s / 1e9,
+        "tokens_per_s": world * per_rank_tokens / per_step_s,
+    }
+
+
+# ---------------------------------------------------------------------------
+# ledger (algorithmic HBM bytes)
+# ---------------------------------------------------------------------------
+
+def ledger(w, n_exp: int, n_valid: int, n_recv: int, fp8: bool = False) -> dict:
+    """Bytes the method must move on one device (reads deduplicated, padding
+    rows included, the dense S*P*H window not counted)."""
+    T, P, E, K, H = w.T, w.P, w.E, w.K, w.H
+    plan = (T * K * 8 + T * P + T * P * 4 + T * K * 4 + n_recv * 4 + n_exp * 4
+            + 4 * (4 * P * P + 2 * P * P * 16 + 3 * E + P))
+    if fp8:
+        dispatch = T * H * 2 + n_exp * (H + 4 * H // 128) + T * K * 4
+    else:
+        dispatch = T * H * 2 + n_exp * H * 2 + T * K * 4
+    combine = n_valid * H * 2 + T * K * (4 + 4) + T * H * 2
+    return {"plan": plan, "dispatch": dispatch, "combine": combine, "total": plan + dispatch + combine}
+
+
+def payload_ledger(w, n_recv: int) -> int:
+    """The pages' 'physical payload' form: received (token, destination) rows
+    times the per-token bytes of x, topk_idx and topk_weights, no padding."""
+    return n_recv * (w.H * 2 + w.K * 8 + w.K * 4)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+        self.windows = []
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50",
+                 "-i", str(self.dev), "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, t0: float, t1: float):
+        self.windows.append((t0, t1))
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if any(a - 0.1 <= r[0] <= b + 0.1 for a, b in self.windows)]
+        use = inside or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {
+            "sm_mhz": statistics.median(r[1] for r in use) if use else None,
+            "sm_max_mhz": max(r[2] for r in use) if use else None,
+            "reasons": reasons,
+            "samples": len(inside),
+        }
+
+
+# ---------------------------------------------------------------------------
+# roofline inputs
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(kernel_file: str) -> str:
+    with open(os.path.join(ROOT, "combine_ep_plan_gb300", "csrc", kernel_file), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, kernel_file: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, if the kernel source has not changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}.{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256") != source_digest(kernel_file):
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_pass(w, idx, wts, x):
+    import oracle
+    pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
+    y = oracle.dispatch_bf16(x, pl, True)
+    oracle.combine(y, pl, wts)
+    return pl
+
+
+def oracle_sample(w, min_seconds: float):
+    """Whole-workload oracle passes until min_seconds of CPU work -> GB/s."""
+    from combine_ep_plan_gb300.inputs import draw_hidden, draw_topk, hidden_seed
+    idx, wts = draw_topk(w)
+    x = draw_hidden(w.T, w.H, hidden_seed(w))
+    times = []
+    pl = None
+    t_start = time.perf_counter()
+    while not times or time.perf_counter() - t_start < min_seconds:
+        t0 = time.perf_counter()
+        pl = oracle_pass(w, idx, wts, x)
+        times.append(time.perf_counter() - t0)
+    n_valid = int(np.sum(pl.slot >= 0))
+    led = ledger(w, pl.num_expanded, n_valid, pl.num_recv_total)
+    t = statistics.mean(times)
+    return {"gbs": led["total"] / t / 1e9, "tokens_per_s": w.T / t, "seconds_per_pass": t, "passes": len(times)}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on the host cores."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from combine_ep_plan_gb300.inputs import WORKLOADS, draw_hidden, draw_topk, hidden_seed
+    full = WORKLOADS[args.workload]
+    # each step is a bounded sample of the workload: fewer tokens per rank, so
+    # that warmup + steps take about two minutes of single-threaded CPU time
+    est_full_s = 4.0 * full.T / 16384 * full.H / 7168
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    S = int(max(8, min(full.S, full.S * budget / est_full_s)))
+    w = full.scaled(S=S)
+    idx, wts = draw_topk(w)
+    x = draw_hidden(w.T, w.H, hidden_seed(w))
+    for _ in range(args.warmup):
+        oracle_pass(w, idx, wts, x)
+    t0 = time.perf_counter()
+    pl = None
+    for _ in range(args.steps):
+        pl = oracle_pass(w, idx, wts, x)
+    dt = time.perf_counter() - t0
+    n_valid = int(np.sum(pl.slot >= 0))
+    led = ledger(w, pl.num_expanded, n_valid, pl.num_recv_total)
+    gbs = led["total"] * args.steps / dt / 1e9
+    sample = f"{args.workload} workload with S={S} tokens/rank (T={w.T}) per step, single-threaded C oracle"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "tokens_per_s": w.T * args.steps / dt,
+        "config": workload_config(full, sample_S=S),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, sample_S=None) -> dict:
+    c = {"workload": f"{w.name}: P={w.P} ranks, E={w.E} experts, S={w.S} tokens/rank (T={w.T}), "
+                     f"H={w.H} bf16, top-{w.K} {w.routing}, expert_alignment={w.A}, fresh plan -> dispatch "
+                     f"(zero padding) -> identity expert -> combine",
+         "ranks": w.P, "experts": w.E, "tokens": w.T, "hidden": w.H, "topk": w.K, "expert_alignment": w.A,
+         "l2": "no flush: inputs larger than L2 (x %.0f MB, expanded rows ~%.2f GB per step)" % (
+             w.T * w.H * 2 / 1e6, w.T * w.K * w.H * 2 / 1e9)}
+    if sample_S is not None:
+        c["sample_tokens_per_rank"] = sample_S
+    return c
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    import combine_ep_plan_gb300 as ep
+    from combine_ep_plan_gb300 import build as ep_build
+    from combine_ep_plan_gb300.inputs import WORKLOADS, bits_to_bf16_tensor, draw_hidden, draw_topk, hidden_seed
+
+    rank, world, local = dist_init(use_cuda=True)
+    torch.cuda.set_device(local)
+    ep_build.build()
+    ep.load_library()
+    w = WORKLOADS[args.workload]
+    idx_np, w_np = draw_topk(w)
+    x_np = draw_hidden(w.T, w.H, hidden_seed(w))
+
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    idx_t = torch.from_numpy(idx_np).to(dev)
+    wts_t = torch.from_numpy(w_np).to(dev)
+    x_t = bits_to_bf16_tensor(x_np).to(dev)
+    cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
+    recv = torch.empty((cap, w.H), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        h = ep.plan(idx_t, w.P, w.E, w.A, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ep.dispatch(h, x_t, "bf16", True, recv_x=recv, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        ep.combine(h, recv, wts_t, out=out, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+        return h
+
+    # sizes for the ledger (outside any timed region)
+    h = step()
+    n_exp, n_recv = h.sizes(stream)
+    h.check(stream)
+    n_valid = int((idx_t >= 0).sum().item())
+    h.destroy(stream)
+    led = ledger(w, n_exp, n_valid, n_recv)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        step().destroy(stream)
+    torch.cuda.synchronize()
+    barrier()
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        step(events[i]).destroy(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    sampler.mark(t_wall0, t_wall1)
+    local_ms = start.elapsed_time(end)
+    plan_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
+    disp_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+    comb_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in events)
+    agg = aggregate(led["total"], w.T, local_ms, world, args.steps)
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # inputs from pinned memory and D2H of its result inside the timed region
+    x_pin = torch.empty_like(x_t, device="cpu").pin_memory()
+    x_pin.copy_(bits_to_bf16_tensor(x_np))
+    idx_pin = torch.from_numpy(idx_np).pin_memory()
+    w_pin = torch.from_numpy(w_np).pin_memory()
+    out_pin = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+
+    def e2e_step():
+        x_t.copy_(x_pin, non_blocking=True)
+        idx_t.copy_(idx_pin, non_blocking=True)
+        wts_t.copy_(w_pin, non_blocking=True)
+        step().destroy(stream)
+        out_pin.copy_(out, non_blocking=True)
+
+    for _ in range(min(3, e2e_steps)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    s2.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    sampler.mark(t_wall0, t_wall1)
+    agg_e2e = aggregate(led["total"], w.T, s2.elapsed_time(e2), world, e2e_steps)
+    clocks = sampler.stop()
+    h2d = x_pin.numel() * 2 + idx_pin.numel() * 8 + w_pin.numel() * 4
+    d2h = out_pin.numel() * 2
+
+    # roofline of the dominant kernel
+    peak, peak_src = hbm_peak()
+    if disp_ms >= comb_ms:
+        kname, kfile, kbytes, kms = "ep_dispatch_bf16_kernel", "ep_dispatch_kernels.cu", led["dispatch"], disp_ms
+    else:
+        kname, kfile, kbytes, kms = "ep_combine_kernel", "ep_combine_kernels.cu", led["combine"], comb_ms
+    achieved = kbytes / (kms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": profiled_traffic(kname, kfile, w.name), "algorithmic_bytes": kbytes}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s = oracle_sample(w, min_seconds=8.0)
+        cpu = {"value": round(s["gbs"], 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"full {w.name} workload (T={w.T}, H={w.H}), {s['passes']} plan+dispatch+combine "
+                         f"pass(es), single-threaded C oracle", "tokens_per_s": round(s["tokens_per_s"], 1)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(agg["gbs"], 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(agg["ms_per_step"], 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded Gumbel-top-k routing, N(0,1) bf16 hidden states)",
+            "tokens_per_s": round(agg["tokens_per_s"], 1),
+            "hbm_roofline_frac": round(agg["gbs"] / world / peak, 4),
+            "config": workload_config(w),
+            "phases_ms": {"plan": round(plan_ms, 5), "dispatch": round(disp_ms, 5), "combine": round(comb_ms, 5)},
+            "ledger_bytes_per_step": led,
+            "payload_gbs": round(world * payload_ledger(w, n_recv) / (agg["ms_per_step"] / 1e3) / 1e9, 2),
+            "roofline": roofline,
+            "e2e": {"value": round(agg_e2e["gbs"], 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(agg_e2e["ms_per_step"], 4),
+                    "tokens_per_s": round(agg_e2e["tokens_per_s"], 1), "steps": e2e_steps,
+                    "api": "C ABI ep_plan/ep_dispatch/ep_combine via the Python binding"},
+            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    barrier()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=800)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="bf16")
+    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, reported as used
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,347 @@
+"""GB300 (sm_103a) MoE expert-parallel routing plan, dispatch and combine.
+
+A thin ctypes binding over the C ABI declared in ``include/ep_plan.h``
+(``libep_gb300.so``, built in-tree by ``combine_ep_plan_gb300.build``).  This
+module only checks and marshals arguments and allocates outputs with torch:
+every step of the plan, dispatch and combine runs in the library's CUDA
+kernels.  There is no CPU or PyTorch fallback: if the library is missing or a
+call fails, an exception is raised.
+
+The P logical ranks of the method live on one GPU: source rank s owns global
+tokens g = s*S + t, expert e lives on rank e // (E/P).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = [
+    "EPError", "EPHandle", "plan", "dispatch", "dispatch_fresh", "dispatch_cached", "combine",
+    "worst_expanded_rows", "library_path", "load_library", "FIELDS", "set_lookback_debug",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libep_gb300.so")
+
+EP_OK, EP_ERR_INVALID, EP_ERR_CAPACITY, EP_ERR_TIMEOUT, EP_ERR_CUDA, EP_ERR_MISMATCH, EP_ERR_OOM = range(7)
+EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
+
+# field name -> (enum value, torch dtype)
+FIELDS = {
+    "is_token_in_rank": (0, torch.uint8),
+    "send_head": (1, torch.int32),
+    "num_tokens_per_rank": (2, torch.int32),
+    "num_tokens_per_expert": (3, torch.int32),
+    "expert_counts": (4, torch.int32),
+    "num_recv": (5, torch.int32),
+    "rank_prefix": (6, torch.int32),
+    "channel_prefix": (7, torch.int32),
+    "recv_channel_prefix": (8, torch.int32),
+    "recv_offsets": (9, torch.int32),
+    "recv_src_idx": (10, torch.int32),
+    "expert_offsets": (11, torch.int32),
+    "slot": (12, torch.int32),
+    "exp_src": (13, torch.int32),
+    "pad_rows": (14, torch.int32),
+}
+
+_TYPESTR = {torch.uint8: "|u1", torch.int32: "<i4"}
+
+
+class EPError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        msg = _lib().ep_status_string(code).decode() if _LIB is not None else f"status {code}"
+        super().__init__(f"{what}: {msg}" if what else msg)
+        self.code = code
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = path or _LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with `python -m combine_ep_plan_gb300.build` "
+            "(there is no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    st = ctypes.c_int
+    lib.ep_abi_version.restype = i32
+    lib.ep_abi_version.argtypes = []
+    lib.ep_status_string.restype = ctypes.c_char_p
+    lib.ep_status_string.argtypes = [st]
+    lib.ep_plan.restype = st
+    lib.ep_plan.argtypes = [vp, i64, i32, i32, i32, i32, i32, vp, ctypes.POINTER(vp)]
+    lib.ep_replan.restype = st
+    lib.ep_replan.argtypes = [vp, vp, vp]
+    lib.ep_plan_sizes.restype = st
+    lib.ep_plan_sizes.argtypes = [vp, vp, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    lib.ep_worst_expanded_rows.restype = i64
+    lib.ep_worst_expanded_rows.argtypes = [i64, i32, i32, i32]
+    lib.ep_dispatch.restype = st
+    lib.ep_dispatch.argtypes = [vp, vp, i64, i32, i32, vp, vp, i64, vp]
+    lib.ep_dispatch_cached.restype = st
+    lib.ep_dispatch_cached.argtypes = [vp, i32, i32, i64, vp, i64, i32, i32, vp, vp, i64, vp]
+    lib.ep_dispatch_fresh.restype = st
+    lib.ep_dispatch_fresh.argtypes = [vp, i64, i32, i32, i32, i32, i32, vp, i64, i32, i32, vp, vp,
+                                      i64, vp, ctypes.POINTER(vp)]
+    lib.ep_combine.restype = st
+    lib.ep_combine.argtypes = [vp, vp, i64, vp, i64, vp, vp]
+    lib.ep_sync_status.restype = st
+    lib.ep_sync_status.argtypes = [vp, vp]
+    lib.ep_handle_get.restype = st
+    lib.ep_handle_get.argtypes = [vp, i32, ctypes.POINTER(vp), ctypes.POINTER(i64), ctypes.POINTER(i32)]
+    lib.ep_handle_info.restype = st
+    lib.ep_handle_info.argtypes = [vp, ctypes.POINTER(i64)] + [ctypes.POINTER(i32)] * 5
+    lib.ep_handle_destroy.restype = st
+    lib.ep_handle_destroy.argtypes = [vp, vp]
+    lib.ep_debug_set_lookback.restype = None
+    lib.ep_debug_set_lookback.argtypes = [i64, i32]
+    _LIB = lib
+    return lib
+
+
+def _lib() -> ctypes.CDLL:
+    return _LIB if _LIB is not None else load_library()
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _check(code: int, what: str):
+    if code != EP_OK:
+        raise EPError(code, what)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+class _ArrayView:
+    """Non-owning device view handed to torch through __cuda_array_interface__."""
+
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {
+            "shape": tuple(int(s) for s in shape), "typestr": typestr,
+            "data": (ptr, False), "version": 3, "strides": None, "stream": None,
+        }
+
+
+class EPHandle:
+    """A routing plan: owns the library handle and its device arrays."""
+
+    def __init__(self, ptr: int, stream: Optional[torch.cuda.Stream]):
+        self._ptr = ptr
+        lib = _lib()
+        S = ctypes.c_int64()
+        P, K, E, A, C = (ctypes.c_int() for _ in range(5))
+        _check(lib.ep_handle_info(ptr, ctypes.byref(S), ctypes.byref(P), ctypes.byref(K),
+                                  ctypes.byref(E), ctypes.byref(A), ctypes.byref(C)), "ep_handle_info")
+        self.S, self.P, self.K, self.E, self.A, self.C = S.value, P.value, K.value, E.value, A.value, C.value
+        self.device = torch.cuda.current_device()
+        self._sizes = None
+
+    @property
+    def T(self) -> int:
+        return self.P * self.S
+
+    @property
+    def ptr(self) -> int:
+        if not self._ptr:
+            raise RuntimeError("handle has been destroyed")
+        return self._ptr
+
+    def field(self, name: str) -> torch.Tensor:
+        """A torch view (no copy) of one plan array; valid while the handle lives."""
+        enum, dtype = FIELDS[name]
+        p = ctypes.c_void_p()
+        shape = (ctypes.c_int64 * 3)()
+        nd = ctypes.c_int()
+        _check(_lib().ep_handle_get(self.ptr, enum, ctypes.byref(p), shape, ctypes.byref(nd)), name)
+        view = _ArrayView(p.value, list(shape)[: nd.value], _TYPESTR[dtype])
+        return torch.as_tensor(view, device=f"cuda:{self.device}")
+
+    def sizes(self, stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:
+        """(N_exp, N_recv); synchronises the stream on first call."""
+        if self._sizes is None:
+            ne, nr = ctypes.c_int64(), ctypes.c_int64()
+            _check(_lib().ep_plan_sizes(self.ptr, _stream_ptr(stream), ctypes.byref(ne), ctypes.byref(nr)),
+                   "ep_plan_sizes")
+            self._sizes = (ne.value, nr.value)
+        return self._sizes
+
+    def replan(self, topk_idx: torch.Tensor, stream: Optional[torch.cuda.Stream] = None):
+        _need(topk_idx, "topk_idx", torch.int64, 2)
+        _check(_lib().ep_replan(self.ptr, topk_idx.data_ptr(), _stream_ptr(stream)), "ep_replan")
+        self._sizes = None
+
+    def sync_status(self, stream: Optional[torch.cuda.Stream] = None) -> int:
+        """Synchronise and return (and clear) the device status code."""
+        return _lib().ep_sync_status(self.ptr, _stream_ptr(stream))
+
+    def check(self, stream: Optional[torch.cuda.Stream] = None):
+        _check(self.sync_status(stream), "device status")
+
+    def destroy(self, stream: Optional[torch.cuda.Stream] = None):
+        if self._ptr:
+            _lib().ep_handle_destroy(self._ptr, _stream_ptr(stream))
+            self._ptr = 0
+
+    def __del__(self):
+        try:
+            if self._ptr and _LIB is not None and torch.cuda.is_initialized():
+                self.destroy()
+        except Exception:
+            pass
+
+
+def plan(topk_idx: torch.Tensor, num_ranks: int, num_experts: int, expert_alignment: int = 1,
+         num_channels: int = 0, stream: Optional[torch.cuda.Stream] = None) -> EPHandle:
+    """Build the routing plan from topk_idx [T,K] int64 (T = num_ranks * S)."""
+    _need(topk_idx, "topk_idx", torch.int64, 2)
+    T, K = topk_idx.shape
+    if T % num_ranks:
+        raise ValueError("topk_idx rows must be a multiple of num_ranks")
+    h = ctypes.c_void_p()
+    _check(_lib().ep_plan(topk_idx.data_ptr(), T // num_ranks, num_ranks, K, num_experts,
+                          expert_alignment, num_channels, _stream_ptr(stream), ctypes.byref(h)), "ep_plan")
+    return EPHandle(h.value, stream)
+
+
+def worst_expanded_rows(num_tokens: int, num_topk: int, num_experts: int, expert_alignment: int) -> int:
+    return int(_lib().ep_worst_expanded_rows(num_tokens, num_topk, num_experts, expert_alignment))
+
+
+def _dispatch_outputs(H, out_dtype, recv_x, recv_scales, capacity, device):
+    if recv_x is None:
+        dt = torch.bfloat16 if out_dtype == "bf16" else torch.float8_e4m3fn
+        recv_x = torch.empty((capacity, H), dtype=dt, device=device)
+    if out_dtype == "fp8" and recv_scales is None:
+        recv_scales = torch.empty((recv_x.shape[0], H // 128), dtype=torch.float32, device=device)
+    return recv_x, recv_scales
+
+
+def _dtype_code(out_dtype: str) -> int:
+    if out_dtype == "bf16":
+        return EP_DTYPE_BF16
+    if out_dtype == "fp8":
+        return EP_DTYPE_FP8_E4M3
+    raise ValueError("out_dtype must be 'bf16' or 'fp8'")
+
+
+def _check_dispatch(x, recv_x, recv_scales, out_dtype):
+    _need(x, "x", torch.bfloat16, 2)
+    want = torch.bfloat16 if out_dtype == "bf16" else torch.float8_e4m3fn
+    _need(recv_x, "recv_x", want, 2)
+    if recv_x.shape[1] != x.shape[1]:
+        raise ValueError("recv_x hidden size differs from x")
+    if out_dtype == "fp8":
+        _need(recv_scales, "recv_scales", torch.float32, 2)
+        if recv_scales.shape[0] < recv_x.shape[0] or recv_scales.shape[1] != x.shape[1] // 128:
+            raise ValueError("recv_scales must be [rows, H/128]")
+
+
+def dispatch(handle: EPHandle, x: torch.Tensor, out_dtype: str = "bf16", zero_pad: bool = True,
+             recv_x: Optional[torch.Tensor] = None, recv_scales: Optional[torch.Tensor] = None,
+             capacity: Optional[int] = None, stream: Optional[torch.cuda.Stream] = None):
+    """Row scatter of x [T,H] bf16 into the expanded layout.
+
+    Without recv_x, the output is allocated with the exact row count, which
+    synchronises the stream once (ep_plan_sizes); pass recv_x (e.g. sized by
+    worst_expanded_rows) to avoid that.  Returns (recv_x, recv_scales|None).
+    """
+    code = _dtype_code(out_dtype)
+    H = x.shape[1]
+    if recv_x is None and capacity is None:
+        capacity = handle.sizes(stream)[0]
+    recv_x, recv_scales = _dispatch_outputs(H, out_dtype, recv_x, recv_scales, capacity, x.device)
+    _check_dispatch(x, recv_x, recv_scales, out_dtype)
+    _check(_lib().ep_dispatch(handle.ptr, x.data_ptr(), H, code, int(bool(zero_pad)), recv_x.data_ptr(),
+                              recv_scales.data_ptr() if recv_scales is not None else None,
+                              recv_x.shape[0], _stream_ptr(stream)), "ep_dispatch")
+    return recv_x, recv_scales
+
+
+def dispatch_cached(handle: EPHandle, x: torch.Tensor, num_experts: int, expert_alignment: int,
+                    num_tokens_per_rank: int, out_dtype: str = "bf16", zero_pad: bool = True,
+                    recv_x: Optional[torch.Tensor] = None, recv_scales: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None):
+    """Cached-handle dispatch: checks (E, A, S) against the handle first."""
+    code = _dtype_code(out_dtype)
+    H = x.shape[1]
+    capacity = handle.sizes(stream)[0] if recv_x is None else None
+    recv_x, recv_scales = _dispatch_outputs(H, out_dtype, recv_x, recv_scales, capacity, x.device)
+    _check_dispatch(x, recv_x, recv_scales, out_dtype)
+    _check(_lib().ep_dispatch_cached(handle.ptr, num_experts, expert_alignment, num_tokens_per_rank,
+                                     x.data_ptr(), H, code, int(bool(zero_pad)), recv_x.data_ptr(),
+                                     recv_scales.data_ptr() if recv_scales is not None else None,
+                                     recv_x.shape[0], _stream_ptr(stream)), "ep_dispatch_cached")
+    return recv_x, recv_scales
+
+
+def dispatch_fresh(topk_idx: torch.Tensor, x: torch.Tensor, num_ranks: int, num_experts: int,
+                   expert_alignment: int = 1, num_channels: int = 0, out_dtype: str = "bf16",
+                   zero_pad: bool = True, recv_x: Optional[torch.Tensor] = None,
+                   recv_scales: Optional[torch.Tensor] = None,
+                   stream: Optional[torch.cuda.Stream] = None):
+    """Plan + dispatch in one library call; outputs default to the worst-case
+    row count (no synchronisation).  Returns (handle, recv_x, recv_scales)."""
+    _need(topk_idx, "topk_idx", torch.int64, 2)
+    code = _dtype_code(out_dtype)
+    T, K = topk_idx.shape
+    H = x.shape[1]
+    cap = worst_expanded_rows(T, K, num_experts, expert_alignment)
+    recv_x, recv_scales = _dispatch_outputs(H, out_dtype, recv_x, recv_scales, cap, x.device)
+    _check_dispatch(x, recv_x, recv_scales, out_dtype)
+    h = ctypes.c_void_p()
+    _check(_lib().ep_dispatch_fresh(topk_idx.data_ptr(), T // num_ranks, num_ranks, K, num_experts,
+                                    expert_alignment, num_channels, x.data_ptr(), H, code,
+                                    int(bool(zero_pad)), recv_x.data_ptr(),
+                                    recv_scales.data_ptr() if recv_scales is not None else None,
+                                    recv_x.shape[0], _stream_ptr(stream), ctypes.byref(h)),
+           "ep_dispatch_fresh")
+    return EPHandle(h.value, stream), recv_x, recv_scales
+
+
+def combine(handle: EPHandle, y: torch.Tensor, topk_weights: torch.Tensor,
+            out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Weighted combine of y [rows,H] bf16 back to [T,H] bf16."""
+    _need(y, "y", torch.bfloat16, 2)
+    _need(topk_weights, "topk_weights", torch.float32, 2)
+    if tuple(topk_weights.shape) != (handle.T, handle.K):
+        raise ValueError("topk_weights must be [T,K]")
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty((handle.T, H), dtype=torch.bfloat16, device=y.device)
+    _need(out, "out", torch.bfloat16, 2)
+    if tuple(out.shape) != (handle.T, H):
+        raise ValueError("out must be [T,H]")
+    _check(_lib().ep_combine(handle.ptr, y.data_ptr(), y.shape[0], topk_weights.data_ptr(), H,
+                             out.data_ptr(), _stream_ptr(stream)), "ep_combine")
+    return out
+
+
+def set_lookback_debug(poll_limit: int = 0, suppress_tile: int = -1):
+    """Test hook for the plan scan's bounded wait (see ep_debug_set_lookback)."""
+    _lib().ep_debug_set_lookback(poll_limit, suppress_tile)

@@ -1,0 +1,410 @@
+// ep_api.cu — the C ABI: argument checks, the plan handle, its device
+// memory layout and the launch sequences.  Host code only.
+//
+// A handle owns one stream-ordered device allocation carved by a cursor into
+// regions (the symmetric-workspace idea of "Ascend DeepEP MoE Dispatch
+// Optimization", section "Workspace 不是一个 Tensor，而是一块地址空间", here a
+// single-device window).  The regions that accumulate (counters, totals,
+// per-source expert counts, look-back descriptors) come first so one memset
+// clears them before each plan.
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "ep_plan.h"
+#include "ep_internal.cuh"
+
+namespace {
+
+constexpr int kAbiVersion = 1;
+constexpr long long kDefaultPollLimit = 1ll << 20;
+
+long long g_poll_limit = kDefaultPollLimit;
+int g_suppress_tile = -1;
+
+struct Layout {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    off = (off + 255) & ~static_cast<size_t>(255);
+    size_t at = off;
+    off += bytes;
+    return at;
+  }
+};
+
+}  // namespace
+
+struct ep_handle_s {
+  ep::PlanDev dev;
+  void* base = nullptr;
+  size_t bytes = 0;
+  size_t zero_bytes = 0;
+  int64_t cap_recv = 0, cap_exp = 0, cap_pad = 0;
+  int device = 0;
+};
+
+namespace ep {
+
+int num_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace ep
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+ep_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return EP_OK;
+  if (e == cudaErrorMemoryAllocation) return EP_ERR_OOM;
+  return EP_ERR_CUDA;
+}
+
+// Keep freed handle memory in the device's default pool, so that planning
+// every step does not return memory to the driver and re-map it.
+void keep_pool_memory(int dev) {
+  static std::once_flag once[64];
+  if (dev < 0 || dev >= 64) return;
+  std::call_once(once[dev], [dev] {
+    cudaMemPool_t pool;
+    if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+      uint64_t thr = UINT64_MAX;
+      cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+    }
+  });
+}
+
+ep_status_t check_shape(int64_t S, int P, int K, int E, int A, int* C) {
+  if (S < 1 || P < 1 || P > EP_MAX_RANKS || E < 1 || E > EP_MAX_EXPERTS || K < 1 ||
+      K > EP_MAX_TOPK || K > E || A < 1)
+    return EP_ERR_INVALID;
+  if (E % P != 0) return EP_ERR_INVALID;
+  if (*C == 0) *C = static_cast<int>(S < EP_DEFAULT_CHANNELS ? S : EP_DEFAULT_CHANNELS);
+  if (*C < 1 || *C > S) return EP_ERR_INVALID;
+  const int64_t T = static_cast<int64_t>(P) * S;
+  if (T > INT32_MAX / 2) return EP_ERR_INVALID;
+  const int64_t worst = T * K + static_cast<int64_t>(E) * (A - 1);
+  if (worst >= INT32_MAX) return EP_ERR_INVALID;
+  return EP_OK;
+}
+
+// Sizes every region and records device pointers relative to `base`.
+size_t layout_handle(ep_handle_s* h, char* base) {
+  ep::PlanDev& p = h->dev;
+  const int64_t T = p.T, P = p.P, E = p.E, K = p.K, C = p.C, A = p.A;
+  Layout L;
+  // zeroed region
+  const size_t o_ctr = L.take(sizeof(unsigned) * ep::kCtrWords);
+  const size_t o_sizes = L.take(sizeof(int) * ep::kSizeWords);
+  const size_t o_totals = L.take(sizeof(int) * (P + E));
+  const size_t o_ntpe = L.take(sizeof(int) * P * E);
+  const size_t o_desc = L.take(sizeof(unsigned long long) * p.num_tiles * (P + E));
+  h->zero_bytes = L.off;
+  // outputs
+  const size_t o_ntpr = L.take(sizeof(int) * P * P);
+  const size_t o_rpm = L.take(sizeof(int) * P * P);
+  const size_t o_cpm = L.take(sizeof(int) * P * P * C);
+  const size_t o_rcpm = L.take(sizeof(int) * P * P * C);
+  const size_t o_roff = L.take(sizeof(int) * (P + 1));
+  const size_t o_eoff = L.take(sizeof(int) * (E + 1));
+  const size_t o_poff = L.take(sizeof(int) * (E + 1));
+  const size_t o_slot = L.take(sizeof(int) * T * K);
+  const size_t o_head = L.take(sizeof(int) * T * P);
+  h->cap_recv = T * (K < P ? K : P);
+  const size_t o_rsrc = L.take(sizeof(int) * h->cap_recv);
+  h->cap_exp = T * K + E * (A - 1);
+  const size_t o_esrc = L.take(sizeof(int) * h->cap_exp);
+  h->cap_pad = E * (A - 1);
+  const size_t o_pads = L.take(sizeof(int) * (h->cap_pad > 0 ? h->cap_pad : 1));
+  const size_t o_inr = L.take(sizeof(unsigned char) * T * P);
+  const size_t total = L.take(0);
+  if (base) {
+    p.ctr = reinterpret_cast<unsigned*>(base + o_ctr);
+    p.sizes = reinterpret_cast<int*>(base + o_sizes);
+    p.totals = reinterpret_cast<int*>(base + o_totals);
+    p.ntpe = reinterpret_cast<int*>(base + o_ntpe);
+    p.desc = reinterpret_cast<unsigned long long*>(base + o_desc);
+    p.ntpr = reinterpret_cast<int*>(base + o_ntpr);
+    p.rpm = reinterpret_cast<int*>(base + o_rpm);
+    p.cpm = reinterpret_cast<int*>(base + o_cpm);
+    p.rcpm = reinterpret_cast<int*>(base + o_rcpm);
+    p.recv_off = reinterpret_cast<int*>(base + o_roff);
+    p.exp_off = reinterpret_cast<int*>(base + o_eoff);
+    p.pad_off = reinterpret_cast<int*>(base + o_poff);
+    p.slot = reinterpret_cast<int*>(base + o_slot);
+    p.send_head = reinterpret_cast<int*>(base + o_head);
+    p.recv_src_idx = reinterpret_cast<int*>(base + o_rsrc);
+    p.exp_src = reinterpret_cast<int*>(base + o_esrc);
+    p.pad_rows = reinterpret_cast<int*>(base + o_pads);
+    p.in_rank = reinterpret_cast<unsigned char*>(base + o_inr);
+  }
+  return total;
+}
+
+ep_status_t enqueue_plan(ep_handle_s* h, const int64_t* topk_idx, cudaStream_t stream) {
+  h->dev.topk_idx = topk_idx;
+  h->dev.poll_limit = g_poll_limit;
+  h->dev.suppress_tile = g_suppress_tile;
+  cudaError_t e = cudaMemsetAsync(h->base, 0, h->zero_bytes, stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  return cuda_status(ep::launch_plan(h->dev, stream));
+}
+
+ep_status_t read_status_word(ep_handle_s* h, cudaStream_t stream, bool clear, int sizes[3]) {
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  unsigned st = 0;
+  e = cudaMemcpy(&st, h->dev.ctr + ep::kCtrStatus, sizeof st, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (sizes) {
+    e = cudaMemcpy(sizes, h->dev.sizes, sizeof(int) * 3, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  if (clear && st) {
+    const unsigned zero = 0;
+    e = cudaMemcpy(h->dev.ctr + ep::kCtrStatus, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  if (st & (ep::kStInvalidId | ep::kStDuplicate)) return EP_ERR_INVALID;
+  if (st & ep::kStTimeout) return EP_ERR_TIMEOUT;
+  if (st & ep::kStCapacity) return EP_ERR_CAPACITY;
+  return EP_OK;
+}
+
+ep_status_t check_dispatch_args(ep_handle_s* h, const void* x, int64_t H, ep_dtype_t out_dtype,
+                                void* recv_x, float* recv_scales, int64_t capacity) {
+  if (!h || !x || !recv_x || capacity < 0 || H < 8 || H % 8 != 0) return EP_ERR_INVALID;
+  if (!aligned(x, 16) || !aligned(recv_x, 16)) return EP_ERR_INVALID;
+  if (out_dtype == EP_DTYPE_BF16) {
+    if (recv_scales) return EP_ERR_INVALID;
+  } else if (out_dtype == EP_DTYPE_FP8_E4M3) {
+    if (H % 128 != 0 || !recv_scales || !aligned(recv_scales, 16)) return EP_ERR_INVALID;
+  } else {
+    return EP_ERR_INVALID;
+  }
+  return EP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ep_abi_version(void) { return kAbiVersion; }
+
+const char* ep_status_string(ep_status_t s) {
+  switch (s) {
+    case EP_OK: return "EP_OK";
+    case EP_ERR_INVALID: return "EP_ERR_INVALID: invalid argument or routing data";
+    case EP_ERR_CAPACITY: return "EP_ERR_CAPACITY: output capacity below the exact need";
+    case EP_ERR_TIMEOUT: return "EP_ERR_TIMEOUT: a bounded device wait gave up";
+    case EP_ERR_CUDA: return "EP_ERR_CUDA: CUDA runtime error";
+    case EP_ERR_MISMATCH: return "EP_ERR_MISMATCH: cached handle shape mismatch";
+    case EP_ERR_OOM: return "EP_ERR_OOM: allocation failed";
+  }
+  return "EP_ERR_UNKNOWN";
+}
+
+ep_status_t ep_plan(const int64_t* topk_idx, int64_t S, int P, int K, int E, int A, int C,
+                    ep_stream_t stream_, ep_handle_t* out) {
+  if (!out) return EP_ERR_INVALID;
+  *out = nullptr;
+  if (!topk_idx || !aligned(topk_idx, 8)) return EP_ERR_INVALID;
+  ep_status_t st = check_shape(S, P, K, E, A, &C);
+  if (st != EP_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  ep_handle_s* h = new (std::nothrow) ep_handle_s();
+  if (!h) return EP_ERR_OOM;
+  ep::PlanDev& p = h->dev;
+  p.S = S;
+  p.T = static_cast<int64_t>(P) * S;
+  p.P = P;
+  p.E = E;
+  p.K = K;
+  p.A = A;
+  p.C = C;
+  p.El = E / P;
+  p.chunk = (S + C - 1) / C;
+  p.num_tiles = static_cast<int>((p.T + ep::kTile - 1) / ep::kTile);
+  p.ncols = P + E;
+  cudaGetDevice(&h->device);
+  keep_pool_memory(h->device);
+  h->bytes = layout_handle(h, nullptr);
+  cudaError_t e = cudaMallocAsync(&h->base, h->bytes, stream);
+  if (e != cudaSuccess) {
+    delete h;
+    return cuda_status(e);
+  }
+  layout_handle(h, static_cast<char*>(h->base));
+  st = enqueue_plan(h, topk_idx, stream);
+  if (st != EP_OK) {
+    cudaFreeAsync(h->base, stream);
+    delete h;
+    return st;
+  }
+  *out = h;
+  return EP_OK;
+}
+
+ep_status_t ep_replan(ep_handle_t h, const int64_t* topk_idx, ep_stream_t stream) {
+  if (!h || !topk_idx || !aligned(topk_idx, 8)) return EP_ERR_INVALID;
+  return enqueue_plan(h, topk_idx, reinterpret_cast<cudaStream_t>(stream));
+}
+
+ep_status_t ep_plan_sizes(ep_handle_t h, ep_stream_t stream, int64_t* n_exp, int64_t* n_recv) {
+  if (!h) return EP_ERR_INVALID;
+  int sizes[3] = {0, 0, 0};
+  ep_status_t st = read_status_word(h, reinterpret_cast<cudaStream_t>(stream), false, sizes);
+  if (st == EP_ERR_CUDA || st == EP_ERR_OOM) return st;
+  if (n_exp) *n_exp = sizes[ep::kSizeExp];
+  if (n_recv) *n_recv = sizes[ep::kSizeRecv];
+  return st;
+}
+
+int64_t ep_worst_expanded_rows(int64_t T, int K, int E, int A) {
+  if (T < 0 || K < 1 || E < 1 || A < 1) return -1;
+  return T * K + static_cast<int64_t>(E) * (A - 1);
+}
+
+ep_status_t ep_dispatch(ep_handle_t h, const void* x, int64_t H, ep_dtype_t out_dtype, int zero_pad,
+                        void* recv_x, float* recv_scales, int64_t capacity, ep_stream_t stream_) {
+  ep_status_t st = check_dispatch_args(h, x, H, out_dtype, recv_x, recv_scales, capacity);
+  if (st != EP_OK) return st;
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  ep::DispatchDev d;
+  d.x = x;
+  d.slot = h->dev.slot;
+  d.pad_rows = h->dev.pad_rows;
+  d.sizes = h->dev.sizes;
+  d.status = h->dev.ctr + ep::kCtrStatus;
+  d.out = recv_x;
+  d.scales = recv_scales;
+  d.T = h->dev.T;
+  d.K = h->dev.K;
+  d.H = H;
+  d.capacity = capacity;
+  d.zero_pad = zero_pad ? 1 : 0;
+  cudaError_t e = out_dtype == EP_DTYPE_BF16 ? ep::launch_dispatch_bf16(d, stream)
+                                              : ep::launch_dispatch_fp8(d, stream);
+  return cuda_status(e);
+}
+
+ep_status_t ep_dispatch_cached(ep_handle_t h, int E, int A, int64_t S, const void* x, int64_t H,
+                               ep_dtype_t out_dtype, int zero_pad, void* recv_x, float* recv_scales,
+                               int64_t capacity, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID;
+  if (h->dev.E != E || h->dev.A != A || h->dev.S != S) return EP_ERR_MISMATCH;
+  return ep_dispatch(h, x, H, out_dtype, zero_pad, recv_x, recv_scales, capacity, stream);
+}
+
+ep_status_t ep_dispatch_fresh(const int64_t* topk_idx, int64_t S, int P, int K, int E, int A, int C,
+                              const void* x, int64_t H, ep_dtype_t out_dtype, int zero_pad,
+                              void* recv_x, float* recv_scales, int64_t capacity,
+                              ep_stream_t stream, ep_handle_t* out) {
+  if (!out) return EP_ERR_INVALID;
+  *out = nullptr;
+  // Check the dispatch arguments before planning so that nothing is enqueued
+  // for a call that cannot run.
+  if (!x || !recv_x || capacity < 0 || H < 8 || H % 8 != 0 || !aligned(x, 16) ||
+      !aligned(recv_x, 16))
+    return EP_ERR_INVALID;
+  if (out_dtype == EP_DTYPE_FP8_E4M3 && (H % 128 != 0 || !recv_scales || !aligned(recv_scales, 16)))
+    return EP_ERR_INVALID;
+  if (out_dtype == EP_DTYPE_BF16 && recv_scales) return EP_ERR_INVALID;
+  if (out_dtype != EP_DTYPE_BF16 && out_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_INVALID;
+  ep_handle_t h = nullptr;
+  ep_status_t st = ep_plan(topk_idx, S, P, K, E, A, C, stream, &h);
+  if (st != EP_OK) return st;
+  st = ep_dispatch(h, x, H, out_dtype, zero_pad, recv_x, recv_scales, capacity, stream);
+  if (st != EP_OK) {
+    ep_handle_destroy(h, stream);
+    return st;
+  }
+  *out = h;
+  return EP_OK;
+}
+
+ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, const float* w, int64_t H,
+                       void* out, ep_stream_t stream) {
+  if (!h || !y || !w || !out || y_rows < 0 || H < 8 || H % 8 != 0) return EP_ERR_INVALID;
+  if (!aligned(y, 16) || !aligned(out, 16) || !aligned(w, 4)) return EP_ERR_INVALID;
+  ep::CombineDev c;
+  c.y = y;
+  c.slot = h->dev.slot;
+  c.weights = w;
+  c.status = h->dev.ctr + ep::kCtrStatus;
+  c.out = out;
+  c.T = h->dev.T;
+  c.K = h->dev.K;
+  c.H = H;
+  c.y_rows = y_rows;
+  return cuda_status(ep::launch_combine(c, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ep_status_t ep_sync_status(ep_handle_t h, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID;
+  return read_status_word(h, reinterpret_cast<cudaStream_t>(stream), true, nullptr);
+}
+
+ep_status_t ep_handle_get(ep_handle_t h, ep_field_t f, const void** ptr, int64_t shape[3], int* ndim) {
+  if (!h || !ptr || !shape || !ndim) return EP_ERR_INVALID;
+  const ep::PlanDev& p = h->dev;
+  const int64_t T = p.T, P = p.P, E = p.E, K = p.K, C = p.C;
+  shape[0] = shape[1] = shape[2] = 1;
+  switch (f) {
+    case EP_FIELD_IS_TOKEN_IN_RANK: *ptr = p.in_rank; shape[0] = T; shape[1] = P; *ndim = 2; break;
+    case EP_FIELD_SEND_HEAD: *ptr = p.send_head; shape[0] = T; shape[1] = P; *ndim = 2; break;
+    case EP_FIELD_NUM_TOKENS_PER_RANK: *ptr = p.ntpr; shape[0] = P; shape[1] = P; *ndim = 2; break;
+    case EP_FIELD_NUM_TOKENS_PER_EXPERT: *ptr = p.ntpe; shape[0] = P; shape[1] = E; *ndim = 2; break;
+    case EP_FIELD_EXPERT_COUNTS: *ptr = p.totals + P; shape[0] = E; *ndim = 1; break;
+    case EP_FIELD_NUM_RECV: *ptr = p.totals; shape[0] = P; *ndim = 1; break;
+    case EP_FIELD_RANK_PREFIX: *ptr = p.rpm; shape[0] = P; shape[1] = P; *ndim = 2; break;
+    case EP_FIELD_CHANNEL_PREFIX: *ptr = p.cpm; shape[0] = P; shape[1] = P; shape[2] = C; *ndim = 3; break;
+    case EP_FIELD_RECV_CHANNEL_PREFIX: *ptr = p.rcpm; shape[0] = P; shape[1] = P; shape[2] = C; *ndim = 3; break;
+    case EP_FIELD_RECV_OFFSETS: *ptr = p.recv_off; shape[0] = P + 1; *ndim = 1; break;
+    case EP_FIELD_RECV_SRC_IDX: *ptr = p.recv_src_idx; shape[0] = h->cap_recv; *ndim = 1; break;
+    case EP_FIELD_EXPERT_OFFSETS: *ptr = p.exp_off; shape[0] = E + 1; *ndim = 1; break;
+    case EP_FIELD_SLOT: *ptr = p.slot; shape[0] = T; shape[1] = K; *ndim = 2; break;
+    case EP_FIELD_EXP_SRC: *ptr = p.exp_src; shape[0] = h->cap_exp; *ndim = 1; break;
+    case EP_FIELD_PAD_ROWS: *ptr = p.pad_rows; shape[0] = h->cap_pad; *ndim = 1; break;
+    default: return EP_ERR_INVALID;
+  }
+  return EP_OK;
+}
+
+ep_status_t ep_handle_info(ep_handle_t h, int64_t* S, int* P, int* K, int* E, int* A, int* C) {
+  if (!h) return EP_ERR_INVALID;
+  if (S) *S = h->dev.S;
+  if (P) *P = h->dev.P;
+  if (K) *K = h->dev.K;
+  if (E) *E = h->dev.E;
+  if (A) *A = h->dev.A;
+  if (C) *C = h->dev.C;
+  return EP_OK;
+}
+
+ep_status_t ep_handle_destroy(ep_handle_t h, ep_stream_t stream) {
+  if (!h) return EP_ERR_INVALID;
+  cudaError_t e = cudaSuccess;
+  if (h->base) e = cudaFreeAsync(h->base, reinterpret_cast<cudaStream_t>(stream));
+  delete h;
+  return cuda_status(e);
+}
+
+void ep_debug_set_lookback(int64_t poll_limit, int suppress_tile) {
+  g_poll_limit = poll_limit > 0 ? poll_limit : kDefaultPollLimit;
+  g_suppress_tile = suppress_tile;
+}
+
+}  // extern "C"

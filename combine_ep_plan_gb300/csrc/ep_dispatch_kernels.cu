@@ -1,0 +1,188 @@
+// ep_dispatch_kernels.cu — the dispatch row scatter on sm_103a.
+//
+// One warp per work item, grid-stride over T source tokens followed by the
+// N_pad padding rows.  A token's hidden row is read from HBM exactly once
+// (16-byte non-allocating loads) and stored to each of its expanded rows
+// (the per-destination dedup of TileLang tutorial ch. 38 §1.3 becomes "one
+// read, K writes" on a single device).  Padding rows are zero-filled when
+// requested (§2.2).  FP8: per 128-element group, amax over the group, scale =
+// amax/448 by IEEE division, codes by IEEE division and the hardware E4M3
+// conversion with round-to-nearest-even and satfinite (§3.6).
+#include <cuda_bf16.h>
+
+#include "ep_internal.cuh"
+
+namespace ep {
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_row(uint4* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Unroll factor: 16-byte vectors per lane loaded before the K stores.
+constexpr int kUnroll = 4;
+
+__global__ void __launch_bounds__(256) ep_dispatch_bf16_kernel(DispatchDev a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t hv = a.H / 8;  // 16-byte vectors per row
+  const int64_t n_pad = a.zero_pad ? a.sizes[kSizePad] : 0;
+  const uint4* x = static_cast<const uint4*>(a.x);
+  uint4* out = static_cast<uint4*>(a.out);
+
+  for (int64_t item = warp; item < a.T + n_pad; item += nwarps) {
+    if (item < a.T) {
+      const int64_t g = item;
+      int my_row = -1;
+      if (lane < a.K) my_row = a.slot[g * a.K + lane];
+      if (my_row >= a.capacity) {
+        atomicOr(a.status, kStCapacity);
+        my_row = -1;
+      }
+      const uint4* src = x + g * hv;
+      for (int64_t v0 = 0; v0 < hv; v0 += 32 * kUnroll) {
+        uint4 buf[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int64_t v = v0 + u * 32 + lane;
+          if (v < hv) buf[u] = ld_stream(src + v);
+        }
+        for (int k = 0; k < a.K; ++k) {
+          const int r = __shfl_sync(0xffffffffu, my_row, k);
+          if (r < 0) continue;
+          uint4* dst = out + static_cast<int64_t>(r) * hv;
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            const int64_t v = v0 + u * 32 + lane;
+            if (v < hv) st_row(dst + v, buf[u]);
+          }
+        }
+      }
+    } else {
+      const int r = a.pad_rows[item - a.T];
+      if (r >= a.capacity) {
+        if (lane == 0) atomicOr(a.status, kStCapacity);
+        continue;
+      }
+      uint4* dst = out + static_cast<int64_t>(r) * hv;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int64_t v = lane; v < hv; v += 32) st_row(dst + v, z);
+    }
+  }
+}
+
+// Two fp32 values -> two E4M3 codes (lo in the low byte), RNE, satfinite.
+__device__ __forceinline__ unsigned short cvt_e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float bf16_lo(unsigned w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(unsigned w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Each lane owns 16 consecutive elements (two 16-byte loads, one 16-byte
+// store of codes); eight lanes form one 128-element scale group.
+__global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const int64_t hv = a.H / 8;     // 16-byte vectors of bf16 per source row
+  const int64_t qv = a.H / 16;    // 16-byte vectors of codes per expanded row
+  const int64_t groups = a.H / 128;
+  const int64_t n_pad = a.zero_pad ? a.sizes[kSizePad] : 0;
+  const uint4* x = static_cast<const uint4*>(a.x);
+  uint4* out = static_cast<uint4*>(a.out);
+
+  for (int64_t item = warp; item < a.T + n_pad; item += nwarps) {
+    if (item < a.T) {
+      const int64_t g = item;
+      int my_row = -1;
+      if (lane < a.K) my_row = a.slot[g * a.K + lane];
+      if (my_row >= a.capacity) {
+        atomicOr(a.status, kStCapacity);
+        my_row = -1;
+      }
+      const uint4* src = x + g * hv;
+      // 32 lanes x 16 elements = 512 elements (4 groups) per step; H % 128 == 0
+      // so a step may be partial only by whole groups of eight lanes.
+      for (int64_t q0 = 0; q0 < qv; q0 += 32) {
+        const int64_t qi = q0 + lane;  // this lane's 16-element chunk
+        const bool active = qi < qv;
+        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+        if (active) {
+          lo = ld_stream(src + 2 * qi);
+          hi = ld_stream(src + 2 * qi + 1);
+        }
+        float f[16];
+        const unsigned w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          f[2 * i] = bf16_lo(w[i]);
+          f[2 * i + 1] = bf16_hi(w[i]);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        const float scale = __fdiv_rn(amax, 448.0f);
+        uint4 q = make_uint4(0u, 0u, 0u, 0u);
+        if (amax != 0.0f) {
+          unsigned short c[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
+          q.x = c[0] | (static_cast<unsigned>(c[1]) << 16);
+          q.y = c[2] | (static_cast<unsigned>(c[3]) << 16);
+          q.z = c[4] | (static_cast<unsigned>(c[5]) << 16);
+          q.w = c[6] | (static_cast<unsigned>(c[7]) << 16);
+        }
+        for (int k = 0; k < a.K; ++k) {
+          const int r = __shfl_sync(0xffffffffu, my_row, k);
+          if (r < 0 || !active) continue;
+          st_row(out + static_cast<int64_t>(r) * qv + qi, q);
+          if ((lane & 7) == 0) a.scales[static_cast<int64_t>(r) * groups + qi / 8] = scale;
+        }
+      }
+    } else {
+      const int r = a.pad_rows[item - a.T];
+      if (r >= a.capacity) {
+        if (lane == 0) atomicOr(a.status, kStCapacity);
+        continue;
+      }
+      uint4* dst = out + static_cast<int64_t>(r) * qv;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int64_t v = lane; v < qv; v += 32) st_row(dst + v, z);
+      for (int64_t j = lane; j < groups; j += 32) a.scales[static_cast<int64_t>(r) * groups + j] = 0.0f;
+    }
+  }
+}
+
+int dispatch_grid() { return num_sms() * 8; }
+
+}  // namespace
+
+cudaError_t launch_dispatch_bf16(const DispatchDev& d, cudaStream_t stream) {
+  ep_dispatch_bf16_kernel<<<dispatch_grid(), 256, 0, stream>>>(d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_fp8(const DispatchDev& d, cudaStream_t stream) {
+  ep_dispatch_fp8_kernel<<<dispatch_grid(), 256, 0, stream>>>(d);
+  return cudaGetLastError();
+}
+
+}  // namespace ep

@@ -1,0 +1,260 @@
+/*
+ * ep_plan.h — C ABI of the GB300 (sm_103a) MoE expert-parallel routing plan,
+ * dispatch row scatter and weighted combine.
+ *
+ * One GPU holds all P logical ranks.  Source rank s owns the global tokens
+ * g = s*S + t (t < S); expert e lives on rank e / (E/P).  Every "transfer" of
+ * the method is an HBM-to-HBM copy inside one device allocation.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev are device pointers; *_host are host pointers.
+ *     The caller owns every input and output buffer it passes.  A handle owns
+ *     the plan arrays it allocates (one device allocation, stream-ordered).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on that stream unless the comment says "synchronises".
+ *   - Host-checkable argument errors return EP_ERR_INVALID (or
+ *     EP_ERR_MISMATCH / EP_ERR_CAPACITY) before anything is enqueued.
+ *     Errors that only the device can see (an expert id out of range, a
+ *     duplicate expert in one token row, an output row beyond the caller's
+ *     capacity, a bounded wait that gave up) are recorded in the handle's
+ *     device status word; no out-of-range row is ever written.  They are
+ *     returned by the next synchronising call (ep_plan_sizes, ep_sync_status).
+ *   - A handle is not thread-safe; calls that use one handle on different
+ *     streams must be ordered by the caller.
+ *
+ * Sources are cited by page title and section:
+ *   [DO] "Ascend DeepEP MoE Dispatch Optimization"
+ *   [TT] TileLang tutorial, chapter 38 "DeepEP-Ascend"
+ */
+#ifndef EP_PLAN_GB300_H
+#define EP_PLAN_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same underlying type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *ep_stream_t;
+
+typedef struct ep_handle_s *ep_handle_t;
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVALID = 1,  /* bad argument, or routing data the method rejects */
+    EP_ERR_CAPACITY = 2, /* an output buffer is smaller than the exact need */
+    EP_ERR_TIMEOUT = 3,  /* a bounded device wait gave up; results are invalid */
+    EP_ERR_CUDA = 4,     /* a CUDA runtime call or kernel launch failed */
+    EP_ERR_MISMATCH = 5, /* cached handle used with different shape parameters */
+    EP_ERR_OOM = 6       /* device or host allocation failed */
+} ep_status_t;
+
+typedef enum {
+    EP_DTYPE_BF16 = 0,     /* bfloat16, 2 bytes */
+    EP_DTYPE_FP8_E4M3 = 1  /* OCP E4M3 ("fn"), 1 byte, with fp32 scales per 128 */
+} ep_dtype_t;
+
+/* Limits of this implementation (checked; EP_ERR_INVALID beyond them). */
+#define EP_MAX_RANKS 1024
+#define EP_MAX_EXPERTS 2048
+#define EP_MAX_TOPK 16
+#define EP_DEFAULT_CHANNELS 16
+
+/* Plan arrays readable through ep_handle_get.  Shapes use T = P*S. */
+typedef enum {
+    EP_FIELD_IS_TOKEN_IN_RANK = 0,  /* [T,P]   uint8: 1 if some expert of g lives on d */
+    EP_FIELD_SEND_HEAD = 1,         /* [T,P]   int32: row of g in d's compact window, -1 if not sent */
+    EP_FIELD_NUM_TOKENS_PER_RANK = 2,   /* [P,P] int32 [s][d]: tokens of s sent to d (dedup) */
+    EP_FIELD_NUM_TOKENS_PER_EXPERT = 3, /* [P,E] int32 [s][e]: (token,slot) pairs of s picking e */
+    EP_FIELD_EXPERT_COUNTS = 4,     /* [E]     int32: n_e, all sources */
+    EP_FIELD_NUM_RECV = 5,          /* [P]     int32: distinct tokens received by d */
+    EP_FIELD_RANK_PREFIX = 6,       /* [P,P]   int32 [s][d]: inclusive sum over sources <= s */
+    EP_FIELD_CHANNEL_PREFIX = 7,    /* [P,P,C] int32 [s][d][c]: inclusive sum over channels <= c */
+    EP_FIELD_RECV_CHANNEL_PREFIX = 8, /* [P,P,C] int32 [d][s][c]: start of segment (s,c) in d's window */
+    EP_FIELD_RECV_OFFSETS = 9,      /* [P+1]   int32: start of d's window in RECV_SRC_IDX */
+    EP_FIELD_RECV_SRC_IDX = 10,     /* [N_recv] int32: source-local token t of each window row */
+    EP_FIELD_EXPERT_OFFSETS = 11,   /* [E+1]   int32: padded start of expert e's rows */
+    EP_FIELD_SLOT = 12,             /* [T,K]   int32: expanded row of (g,k), -1 for an unused slot */
+    EP_FIELD_EXP_SRC = 13,          /* [N_exp] int32: source token g of each expanded row, -1 on padding */
+    EP_FIELD_PAD_ROWS = 14,         /* [N_pad] int32: the padding rows of the expanded layout */
+    EP_FIELD_COUNT = 15
+} ep_field_t;
+
+/* Version of this ABI (bumped on any incompatible change). */
+int ep_abi_version(void);
+
+/* Human-readable name of a status code (static storage). */
+const char *ep_status_string(ep_status_t status);
+
+/*
+ * ep_plan — build the routing plan of one MoE layer.
+ *
+ * Defines: the six-tensor dispatch handle ([DO] "从 Python 接口进入真实调用链",
+ * the handle table: rank_prefix_matrix, channel_prefix_matrix,
+ * recv_channel_prefix_matrix, recv_src_idx, is_token_in_rank, send_head);
+ * the counts and prefixes the notify stage produces ([DO] "Notify 先交换数量和
+ * 前缀"); per-destination dedup ([TT] §1.3); the expanded layout padded to
+ * expert_alignment ([TT] §2.2) in the deterministic order of [TT] §3.5.
+ *
+ * topk_idx_dev        [T,K] int64, row-major, 8-byte aligned.  Entry -1 marks
+ *                     an unused slot; other entries must be distinct experts
+ *                     in [0,E) (device-checked, EP_ERR_INVALID on sync).
+ *                     Read during the call only; the handle keeps no reference.
+ * num_tokens_per_rank S >= 1; T = P*S.
+ * num_ranks           P, 1..EP_MAX_RANKS, E % P == 0.
+ * num_topk            K, 1..min(E, EP_MAX_TOPK).
+ * num_experts         E, 1..EP_MAX_EXPERTS.
+ * expert_alignment    A >= 1: each expert segment is padded to a multiple of A.
+ * num_channels        C in 1..S, or 0 for min(EP_DEFAULT_CHANNELS, S).  Channel c
+ *                     of a source covers tokens [c*ceil(S/C), min(S,(c+1)*ceil(S/C))).
+ * out_handle_host     receives the new handle (NULL on error).
+ * The expanded-row count N_exp must fit int32 (checked on the worst case).
+ */
+ep_status_t ep_plan(const int64_t *topk_idx_dev, int64_t num_tokens_per_rank,
+                    int num_ranks, int num_topk, int num_experts,
+                    int expert_alignment, int num_channels, ep_stream_t stream,
+                    ep_handle_t *out_handle_host);
+
+/*
+ * ep_replan — rebuild the plan of an existing handle for new routing with the
+ * same shape (S, P, K, E, A, C), reusing its device memory: a fresh plan with
+ * no allocation.  Same inputs and checks as ep_plan.
+ */
+ep_status_t ep_replan(ep_handle_t handle, const int64_t *topk_idx_dev, ep_stream_t stream);
+
+/*
+ * ep_plan_sizes — synchronises `stream`, then returns the exact expanded-row
+ * count N_exp (sum over e of ceil(n_e/A)*A) and compact receive-row count
+ * N_recv (sum over d of num_recv[d]); the do_cpu_sync path of the pages
+ * ([DO] "输出长度有动态和固定两种模式").  Returns the device status too.
+ * Either output pointer may be NULL.
+ */
+ep_status_t ep_plan_sizes(ep_handle_t handle, ep_stream_t stream,
+                          int64_t *num_expanded_host, int64_t *num_recv_host);
+
+/*
+ * ep_worst_expanded_rows — an upper bound of N_exp without any device read:
+ * T*K + E*(A-1), the fixed-output-length (num_worst_tokens) path of the pages
+ * ([DO] "输出长度有动态和固定两种模式").  Returns -1 on invalid arguments.
+ */
+int64_t ep_worst_expanded_rows(int64_t num_tokens, int num_topk, int num_experts,
+                               int expert_alignment);
+
+/*
+ * ep_dispatch — the row scatter: each token's hidden row is read once and
+ * written to every expanded row of its (token, slot) pairs, which groups rows
+ * by expert and pads each segment to A rows ([TT] §2.2, §4.3 local copy).
+ *
+ * x_dev          [T,H] bfloat16, 16-byte aligned, H % 8 == 0.
+ * hidden         H.
+ * out_dtype      EP_DTYPE_BF16: recv_x is [capacity_rows,H] bfloat16, a bit copy.
+ *                EP_DTYPE_FP8_E4M3: quantised inside dispatch ([TT] §3.6):
+ *                per row and per 128 elements, scale = amax/448 (IEEE fp32
+ *                division), code = E4M3(x/scale) rounded to nearest even with
+ *                saturation; amax == 0 gives scale 0 and zero codes.  recv_x is
+ *                [capacity_rows,H] E4M3 bytes, recv_scales_dev [capacity_rows,H/128]
+ *                fp32 row-major.  Needs H % 128 == 0.
+ * zero_pad       nonzero: padding rows are zero (codes and scales); 0: padding
+ *                rows are left untouched ([TT] §2.2, do_zero_padding).
+ * recv_x_dev     output, 16-byte aligned.  Rows >= N_exp are never written.
+ * recv_scales_dev output for FP8, 16-byte aligned; must be NULL for BF16.
+ * capacity_rows  rows available in recv_x (and recv_scales).  A capacity below
+ *                N_exp records EP_ERR_CAPACITY and writes no row at or beyond it.
+ * Reusing a handle on new x is the cached dispatch of [TT] §2.4: no plan work.
+ */
+ep_status_t ep_dispatch(ep_handle_t handle, const void *x_dev, int64_t hidden,
+                        ep_dtype_t out_dtype, int zero_pad, void *recv_x_dev,
+                        float *recv_scales_dev, int64_t capacity_rows,
+                        ep_stream_t stream);
+
+/*
+ * ep_dispatch_cached — ep_dispatch on an existing handle after checking that
+ * (num_experts, expert_alignment, num_tokens_per_rank) are the ones the
+ * handle was planned with, as the cached-handle path of [TT] §2.4 asserts.
+ * A difference returns EP_ERR_MISMATCH and enqueues nothing.
+ */
+ep_status_t ep_dispatch_cached(ep_handle_t handle, int num_experts, int expert_alignment,
+                               int64_t num_tokens_per_rank, const void *x_dev,
+                               int64_t hidden, ep_dtype_t out_dtype, int zero_pad,
+                               void *recv_x_dev, float *recv_scales_dev,
+                               int64_t capacity_rows, ep_stream_t stream);
+
+/*
+ * ep_dispatch_fresh — ep_plan followed by ep_dispatch in one call (a fresh
+ * dispatch that re-plans the routing, [DO] "Fresh dispatch 是什么意思").  On
+ * success *out_handle_host holds the new plan for later cached dispatches and
+ * combines.  Arguments as for ep_plan and ep_dispatch.
+ */
+ep_status_t ep_dispatch_fresh(const int64_t *topk_idx_dev, int64_t num_tokens_per_rank,
+                              int num_ranks, int num_topk, int num_experts,
+                              int expert_alignment, int num_channels, const void *x_dev,
+                              int64_t hidden, ep_dtype_t out_dtype, int zero_pad,
+                              void *recv_x_dev, float *recv_scales_dev,
+                              int64_t capacity_rows, ep_stream_t stream,
+                              ep_handle_t *out_handle_host);
+
+/*
+ * ep_combine — the inverse of dispatch ([TT] §2.3): gather each token's
+ * expert outputs back to token order and reduce them with the top-k weights.
+ * out[g,:] = bf16_RNE( sum over k = 0..K-1 with slot[g,k] >= 0, in that
+ * order, of fmaf(w[g,k], float(y[slot[g,k],:]), acc) ), acc starting at 0;
+ * fp32 accumulation, rounded once ([TT] §4.5).  A token with no valid slot
+ * gives zeros.  Padding rows of y are never read.
+ *
+ * y_dev          [y_rows,H] bfloat16 expert outputs in the expanded layout,
+ *                16-byte aligned, H % 8 == 0.  y_rows < N_exp records
+ *                EP_ERR_CAPACITY (rows beyond y_rows are not read).
+ * topk_weights_dev [T,K] float32.
+ * out_dev        [T,H] bfloat16, 16-byte aligned.
+ */
+ep_status_t ep_combine(ep_handle_t handle, const void *y_dev, int64_t y_rows,
+                       const float *topk_weights_dev, int64_t hidden, void *out_dev,
+                       ep_stream_t stream);
+
+/*
+ * ep_sync_status — synchronises `stream`, returns the first error recorded in
+ * the handle's device status word (EP_OK if none) and clears it.
+ */
+ep_status_t ep_sync_status(ep_handle_t handle, ep_stream_t stream);
+
+/*
+ * ep_handle_get — device pointer and shape of one plan array (see ep_field_t).
+ * The pointer stays valid until the handle is destroyed or re-planned; the
+ * arrays are written by kernels on the plan's stream.  shape_host receives up
+ * to 3 extents (unused ones are 1) and *ndim_host the rank of the array; for
+ * RECV_SRC_IDX, EXP_SRC and PAD_ROWS the extent is the allocated capacity and
+ * the valid prefix is given by ep_plan_sizes / expert and pad counts.
+ */
+ep_status_t ep_handle_get(ep_handle_t handle, ep_field_t field, const void **dev_ptr_host,
+                          int64_t shape_host[3], int *ndim_host);
+
+/*
+ * ep_handle_info — the plan's shape: S, P, K, E, A, C (any pointer may be NULL).
+ */
+ep_status_t ep_handle_info(ep_handle_t handle, int64_t *num_tokens_per_rank, int *num_ranks,
+                           int *num_topk, int *num_experts, int *expert_alignment,
+                           int *num_channels);
+
+/*
+ * ep_handle_destroy — release the handle.  Its device memory is freed in
+ * stream order on `stream` (after work already enqueued there).
+ */
+ep_status_t ep_handle_destroy(ep_handle_t handle, ep_stream_t stream);
+
+/*
+ * ep_debug_set_lookback — test hook for the bounded wait of the plan's
+ * single-pass scan.  poll_limit > 0 sets how many times a tile polls a
+ * predecessor's descriptor before it gives up and records EP_ERR_TIMEOUT
+ * (0 restores the default); suppress_tile >= 0 makes that tile never publish
+ * its descriptors, so that its successor's wait runs out (-1 disables).
+ * Process-wide; affects plans enqueued afterwards.
+ */
+void ep_debug_set_lookback(int64_t poll_limit, int suppress_tile);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_PLAN_GB300_H */

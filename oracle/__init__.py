@@ -74,6 +74,8 @@ def _load():
         lib.ep_oracle_combine.restype = None
         lib.ep_oracle_expert_scale.argtypes = [P, i64, P, P, i32, P]
         lib.ep_oracle_expert_scale.restype = None
+        lib.ep_oracle_expert_scale_rows.argtypes = [P, i64, P, i64, i32, P]
+        lib.ep_oracle_expert_scale_rows.restype = None
         lib.ep_oracle_expert_dequant.argtypes = [P, P, i64, i64, P]
         lib.ep_oracle_expert_dequant.restype = None
         lib.ep_oracle_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -220,6 +222,15 @@ def expert_scale(x_exp_bits: np.ndarray, pl: Plan) -> np.ndarray:
     H = x.shape[1]
     y = np.zeros_like(x)
     _load().ep_oracle_expert_scale(_ptr(x), H, _ptr(pl.exp_src), _ptr(pl.expert_offsets), pl.E, _ptr(y))
+    return y
+
+
+def expert_scale_rows(x_rows_bits: np.ndarray, row_expert: np.ndarray, E: int) -> np.ndarray:
+    x = np.ascontiguousarray(x_rows_bits, dtype=np.uint16)
+    re = np.ascontiguousarray(row_expert, dtype=np.int32)
+    n, H = x.shape
+    y = np.zeros_like(x)
+    _load().ep_oracle_expert_scale_rows(_ptr(x), H, _ptr(re), n, E, _ptr(y))
     return y
 
 

@@ -449,3 +449,18 @@ void ep_oracle_expert_dequant(const uint8_t *q, const float *scales, int64_t H,
         for (int64_t h = 0; h < H; ++h)
             y[r * H + h] = ep_oracle_f32_to_bf16(ep_oracle_e4m3_to_f32(q[r * H + h]) * scales[r * G + h / 128]);
 }
+
+/* The same scaling expert on a list of rows whose experts are given
+ * explicitly (row_expert[i] < 0 marks a padding row). */
+void ep_oracle_expert_scale_rows(const uint16_t *x_rows, int64_t H, const int32_t *row_expert,
+                                 int64_t n_rows, int E, uint16_t *y)
+{
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int e = row_expert[r];
+        float f = e >= 0 ? 1.0f + (float)e / (float)E : 0.0f;
+        for (int64_t h = 0; h < H; ++h)
+            y[r * H + h] = e >= 0
+                ? ep_oracle_f32_to_bf16(ep_oracle_bf16_to_f32(x_rows[r * H + h]) * f)
+                : 0;
+    }
+}

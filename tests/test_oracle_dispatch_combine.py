@@ -161,3 +161,14 @@ def test_combine_token_without_slots_is_zero():
     pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
     out = oracle.combine(oracle.dispatch_bf16(x, pl), pl, wts)
     assert not out[10].any()
+
+
+def test_expert_scale_rows_matches_segment_form():
+    w = CASES[4]
+    idx, wts, x, pl = _setup(w)
+    xe = oracle.dispatch_bf16(x, pl)
+    seg = oracle.expert_scale(xe, pl)
+    rows = np.arange(pl.num_expanded)
+    e_of_row = (np.searchsorted(pl.expert_offsets, rows, side="right") - 1).astype(np.int32)
+    e_of_row[pl.exp_src < 0] = -1
+    assert np.array_equal(oracle.expert_scale_rows(xe, e_of_row, w.E), seg)
