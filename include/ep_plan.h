@@ -244,6 +244,64 @@ ep_status_t ep_handle_info(ep_handle_t handle, int64_t *num_tokens_per_rank, int
 ep_status_t ep_handle_destroy(ep_handle_t handle, ep_stream_t stream);
 
 /*
+ * ep_plan_static_scratch — the routing plan without any device allocation.
+ * The source pages have no counterpart: this entry exists for callers that
+ * cannot allocate device memory when they plan, such as a serving runtime
+ * that hands all device memory to its own arena at start-up, or a
+ * latency-critical loop where an allocation may block on the device or fail
+ * under fragmentation.  It computes exactly what ep_plan computes, with the
+ * same kernels, but writes every plan array into buffers the caller owns
+ * (ep_plan_buffers_t) and keeps its scratch (look-back descriptors, counters,
+ * column totals) in one fixed array in the library's device memory,
+ * EP_STATIC_SCRATCH_BYTES large, which every GPU that loads the library holds
+ * until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine; it enqueues memsets, the plan kernels and small
+ * device-to-device copies on `stream`.
+ *
+ * - The first call on a device looks up the scratch array's device address
+ *   (cudaGetSymbolAddress, with that device current); make that first call
+ *   before any stream capture.
+ * - All calls on a device share the one scratch array, and it keeps the last
+ *   call's contents; each call clears what it needs.  Calls whose work
+ *   overlaps on the GPU (other streams, other threads) race on the scratch:
+ *   order them.
+ * - Scratch need: about 8*ceil(T/256)*(P+E) + 4*(P+2E) + 1 KB bytes; a plan
+ *   that would need more than EP_STATIC_SCRATCH_BYTES returns
+ *   EP_ERR_CAPACITY before anything is enqueued (16384 tokens with P+E = 384
+ *   need about 0.2 MB; the limit allows e.g. 65536 tokens with P+E = 1900).
+ * - Arguments and shape limits are those of ep_plan; out and all its pointers
+ *   must be non-NULL device pointers, 4-byte aligned except the uint8 array.
+ *   out->info receives {N_recv, N_exp, N_pad, device status bits}; status
+ *   bit 1 = expert id out of range, 2 = duplicate expert in a row, 8 = a
+ *   bounded wait gave up (the plan is then invalid).
+ */
+#define EP_STATIC_SCRATCH_BYTES (4u << 20)
+
+typedef struct {
+    uint8_t *is_token_in_rank;      /* [T,P] */
+    int32_t *send_head;             /* [T,P] */
+    int32_t *num_tokens_per_rank;   /* [P,P] */
+    int32_t *num_tokens_per_expert; /* [P,E] */
+    int32_t *expert_counts;         /* [E] */
+    int32_t *num_recv;              /* [P] */
+    int32_t *rank_prefix;           /* [P,P] */
+    int32_t *channel_prefix;        /* [P,P,C] */
+    int32_t *recv_channel_prefix;   /* [P,P,C] */
+    int32_t *recv_offsets;          /* [P+1] */
+    int32_t *recv_src_idx;          /* [T*min(K,P)] (valid prefix N_recv) */
+    int32_t *expert_offsets;        /* [E+1] */
+    int32_t *slot;                  /* [T,K] */
+    int32_t *exp_src;               /* [T*K + E*(A-1)] (valid prefix N_exp) */
+    int32_t *pad_rows;              /* [max(1, E*(A-1))] (valid prefix N_pad) */
+    int32_t *info;                  /* [4]: N_recv, N_exp, N_pad, status bits */
+} ep_plan_buffers_t;
+
+ep_status_t ep_plan_static_scratch(const int64_t *topk_idx_dev, int64_t num_tokens_per_rank,
+                                   int num_ranks, int num_topk, int num_experts,
+                                   int expert_alignment, int num_channels,
+                                   const ep_plan_buffers_t *out_dev_buffers, ep_stream_t stream);
+
+/*
  * ep_debug_set_lookback — test hook for the bounded wait of the plan's
  * single-pass scan.  poll_limit > 0 sets how many times a tile polls a
  * predecessor's descriptor before it gives up and records EP_ERR_TIMEOUT
