@@ -294,6 +294,7 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, int64_t H, ep_dtype_t out_
   d.K = h->dev.K;
   d.H = H;
   d.capacity = capacity;
+  d.max_pad = zero_pad ? h->cap_pad : 0;
   d.zero_pad = zero_pad ? 1 : 0;
   cudaError_t e = out_dtype == EP_DTYPE_BF16 ? ep::launch_dispatch_bf16(d, stream)
                                               : ep::launch_dispatch_fp8(d, stream);

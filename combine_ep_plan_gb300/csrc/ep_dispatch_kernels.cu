@@ -32,18 +32,26 @@ __device__ __forceinline__ void st_row(uint4* p, const uint4& v) {
 // Unroll factor: 16-byte vectors per lane loaded before the K stores.
 constexpr int kUnroll = 4;
 
+// Work item = (row item, column chunk of 32*kUnroll vectors): T token rows
+// then N_pad padding rows, each cut into chunks, so that every warp gets many
+// small items and the kernel has no long tail.
 __global__ void __launch_bounds__(256) ep_dispatch_bf16_kernel(DispatchDev a) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const int64_t hv = a.H / 8;  // 16-byte vectors per row
+  constexpr int kChunk = 32 * kUnroll;
+  const int64_t chunks = (hv + kChunk - 1) / kChunk;
   const int64_t n_pad = a.zero_pad ? a.sizes[kSizePad] : 0;
+  const int64_t n_items = (a.T + n_pad) * chunks;
   const uint4* x = static_cast<const uint4*>(a.x);
   uint4* out = static_cast<uint4*>(a.out);
 
-  for (int64_t item = warp; item < a.T + n_pad; item += nwarps) {
-    if (item < a.T) {
-      const int64_t g = item;
+  for (int64_t item = warp; item < n_items; item += nwarps) {
+    const int64_t ri = item / chunks;
+    const int64_t v0 = (item - ri * chunks) * kChunk;
+    if (ri < a.T) {
+      const int64_t g = ri;
       int my_row = -1;
       if (lane < a.K) my_row = a.slot[g * a.K + lane];
       if (my_row >= a.capacity) {
@@ -51,33 +59,35 @@ __global__ void __launch_bounds__(256) ep_dispatch_bf16_kernel(DispatchDev a) {
         my_row = -1;
       }
       const uint4* src = x + g * hv;
-      for (int64_t v0 = 0; v0 < hv; v0 += 32 * kUnroll) {
-        uint4 buf[kUnroll];
+      uint4 buf[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t v = v0 + u * 32 + lane;
+        if (v < hv) buf[u] = ld_stream(src + v);
+      }
+      for (int k = 0; k < a.K; ++k) {
+        const int r = __shfl_sync(0xffffffffu, my_row, k);
+        if (r < 0) continue;
+        uint4* dst = out + static_cast<int64_t>(r) * hv;
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int64_t v = v0 + u * 32 + lane;
-          if (v < hv) buf[u] = ld_stream(src + v);
-        }
-        for (int k = 0; k < a.K; ++k) {
-          const int r = __shfl_sync(0xffffffffu, my_row, k);
-          if (r < 0) continue;
-          uint4* dst = out + static_cast<int64_t>(r) * hv;
-#pragma unroll
-          for (int u = 0; u < kUnroll; ++u) {
-            const int64_t v = v0 + u * 32 + lane;
-            if (v < hv) st_row(dst + v, buf[u]);
-          }
+          if (v < hv) st_row(dst + v, buf[u]);
         }
       }
     } else {
-      const int r = a.pad_rows[item - a.T];
+      const int r = a.pad_rows[ri - a.T];
       if (r >= a.capacity) {
         if (lane == 0) atomicOr(a.status, kStCapacity);
         continue;
       }
       uint4* dst = out + static_cast<int64_t>(r) * hv;
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int64_t v = lane; v < hv; v += 32) st_row(dst + v, z);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t v = v0 + u * 32 + lane;
+        if (v < hv) st_row(dst + v, z);
+      }
     }
   }
 }
@@ -93,7 +103,8 @@ __device__ __forceinline__ float bf16_lo(unsigned w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(unsigned w) { return __uint_as_float(w & 0xffff0000u); }
 
 // Each lane owns 16 consecutive elements (two 16-byte loads, one 16-byte
-// store of codes); eight lanes form one 128-element scale group.
+// store of codes); eight lanes form one 128-element scale group.  Work item =
+// (row item, chunk of 512 elements), T token rows then N_pad padding rows.
 __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -101,13 +112,19 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
   const int64_t hv = a.H / 8;     // 16-byte vectors of bf16 per source row
   const int64_t qv = a.H / 16;    // 16-byte vectors of codes per expanded row
   const int64_t groups = a.H / 128;
+  const int64_t chunks = (qv + 31) / 32;
   const int64_t n_pad = a.zero_pad ? a.sizes[kSizePad] : 0;
+  const int64_t n_items = (a.T + n_pad) * chunks;
   const uint4* x = static_cast<const uint4*>(a.x);
   uint4* out = static_cast<uint4*>(a.out);
 
-  for (int64_t item = warp; item < a.T + n_pad; item += nwarps) {
-    if (item < a.T) {
-      const int64_t g = item;
+  for (int64_t item = warp; item < n_items; item += nwarps) {
+    const int64_t ri = item / chunks;
+    const int64_t qi = (item - ri * chunks) * 32 + lane;  // this lane's 16-element chunk
+    // H % 128 == 0, so an inactive lane takes a whole group of eight lanes with it
+    const bool active = qi < qv;
+    if (ri < a.T) {
+      const int64_t g = ri;
       int my_row = -1;
       if (lane < a.K) my_row = a.slot[g * a.K + lane];
       if (my_row >= a.capacity) {
@@ -115,73 +132,77 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
         my_row = -1;
       }
       const uint4* src = x + g * hv;
-      // 32 lanes x 16 elements = 512 elements (4 groups) per step; H % 128 == 0
-      // so a step may be partial only by whole groups of eight lanes.
-      for (int64_t q0 = 0; q0 < qv; q0 += 32) {
-        const int64_t qi = q0 + lane;  // this lane's 16-element chunk
-        const bool active = qi < qv;
-        uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-        if (active) {
-          lo = ld_stream(src + 2 * qi);
-          hi = ld_stream(src + 2 * qi + 1);
-        }
-        float f[16];
-        const unsigned w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+      uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+      if (active) {
+        lo = ld_stream(src + 2 * qi);
+        hi = ld_stream(src + 2 * qi + 1);
+      }
+      float f[16];
+      const unsigned w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          f[2 * i] = bf16_lo(w[i]);
-          f[2 * i + 1] = bf16_hi(w[i]);
-        }
-        float amax = 0.0f;
+      for (int i = 0; i < 8; ++i) {
+        f[2 * i] = bf16_lo(w[i]);
+        f[2 * i + 1] = bf16_hi(w[i]);
+      }
+      float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-        const float scale = __fdiv_rn(amax, 448.0f);
-        uint4 q = make_uint4(0u, 0u, 0u, 0u);
-        if (amax != 0.0f) {
-          unsigned short c[8];
+      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+      const float scale = __fdiv_rn(amax, 448.0f);
+      uint4 q = make_uint4(0u, 0u, 0u, 0u);
+      if (amax != 0.0f) {
+        unsigned short c[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
-          q.x = c[0] | (static_cast<unsigned>(c[1]) << 16);
-          q.y = c[2] | (static_cast<unsigned>(c[3]) << 16);
-          q.z = c[4] | (static_cast<unsigned>(c[5]) << 16);
-          q.w = c[6] | (static_cast<unsigned>(c[7]) << 16);
-        }
-        for (int k = 0; k < a.K; ++k) {
-          const int r = __shfl_sync(0xffffffffu, my_row, k);
-          if (r < 0 || !active) continue;
-          st_row(out + static_cast<int64_t>(r) * qv + qi, q);
-          if ((lane & 7) == 0) a.scales[static_cast<int64_t>(r) * groups + qi / 8] = scale;
-        }
+        for (int i = 0; i < 8; ++i)
+          c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
+        q.x = c[0] | (static_cast<unsigned>(c[1]) << 16);
+        q.y = c[2] | (static_cast<unsigned>(c[3]) << 16);
+        q.z = c[4] | (static_cast<unsigned>(c[5]) << 16);
+        q.w = c[6] | (static_cast<unsigned>(c[7]) << 16);
+      }
+      for (int k = 0; k < a.K; ++k) {
+        const int r = __shfl_sync(0xffffffffu, my_row, k);
+        if (r < 0 || !active) continue;
+        st_row(out + static_cast<int64_t>(r) * qv + qi, q);
+        if ((lane & 7) == 0) a.scales[static_cast<int64_t>(r) * groups + qi / 8] = scale;
       }
     } else {
-      const int r = a.pad_rows[item - a.T];
+      const int r = a.pad_rows[ri - a.T];
       if (r >= a.capacity) {
         if (lane == 0) atomicOr(a.status, kStCapacity);
         continue;
       }
-      uint4* dst = out + static_cast<int64_t>(r) * qv;
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int64_t v = lane; v < qv; v += 32) st_row(dst + v, z);
-      for (int64_t j = lane; j < groups; j += 32) a.scales[static_cast<int64_t>(r) * groups + j] = 0.0f;
+      if (active) {
+        st_row(out + static_cast<int64_t>(r) * qv + qi, make_uint4(0u, 0u, 0u, 0u));
+        if ((lane & 7) == 0) a.scales[static_cast<int64_t>(r) * groups + qi / 8] = 0.0f;
+      }
     }
   }
 }
 
-int dispatch_grid() { return num_sms() * 8; }
+// One warp per work item: the grid covers the worst-case item count (T rows
+// plus E*(A-1) padding rows, in chunks); warps without an item exit at once.
+// Many short-lived CTAs, balanced by the hardware block scheduler, keep more
+// stores in flight than a resident grid looping over the items.
+unsigned item_grid(int64_t rows, int64_t chunks) {
+  const int64_t warps = rows * chunks;
+  const int64_t blocks = (warps + 7) / 8;
+  return static_cast<unsigned>(blocks < 1 ? 1 : (blocks > 0x7fffffff ? 0x7fffffff : blocks));
+}
 
 }  // namespace
 
 cudaError_t launch_dispatch_bf16(const DispatchDev& d, cudaStream_t stream) {
-  ep_dispatch_bf16_kernel<<<dispatch_grid(), 256, 0, stream>>>(d);
+  const int64_t chunks = (d.H / 8 + 32 * kUnroll - 1) / (32 * kUnroll);
+  ep_dispatch_bf16_kernel<<<item_grid(d.T + d.max_pad, chunks), 256, 0, stream>>>(d);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dispatch_fp8(const DispatchDev& d, cudaStream_t stream) {
-  ep_dispatch_fp8_kernel<<<dispatch_grid(), 256, 0, stream>>>(d);
+  const int64_t chunks = (d.H / 16 + 31) / 32;
+  ep_dispatch_fp8_kernel<<<item_grid(d.T + d.max_pad, chunks), 256, 0, stream>>>(d);
   return cudaGetLastError();
 }
 

@@ -84,6 +84,7 @@ struct DispatchDev {
   int K;
   int64_t H;
   int64_t capacity;
+  int64_t max_pad;        // upper bound of N_pad: E*(A-1) (sizes the grid)
   int zero_pad;
 };
 cudaError_t launch_dispatch_bf16(const DispatchDev& d, cudaStream_t stream);
