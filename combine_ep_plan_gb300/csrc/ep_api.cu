@@ -4,9 +4,10 @@
 // A handle owns one stream-ordered device allocation carved by a cursor into
 // regions (the symmetric-workspace idea of "Ascend DeepEP MoE Dispatch
 // Optimization", section "Workspace 不是一个 Tensor，而是一块地址空间", here a
-// single-device window).  The regions that accumulate (counters, totals,
-// per-source expert counts, look-back descriptors) come first so one memset
-// clears them before each plan.
+// single-device window).  Only the control words and the look-back
+// descriptors are cleared, once, when the handle is made: each plan tags its
+// descriptors with a new epoch, and every other array is fully written by
+// each plan.
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -43,6 +44,7 @@ struct ep_handle_s {
   size_t zero_bytes = 0;
   int64_t cap_recv = 0, cap_exp = 0, cap_pad = 0;
   int device = 0;
+  unsigned epoch = 0;
 };
 
 namespace ep {
@@ -105,13 +107,17 @@ size_t layout_handle(ep_handle_s* h, char* base) {
   ep::PlanDev& p = h->dev;
   const int64_t T = p.T, P = p.P, E = p.E, K = p.K, C = p.C, A = p.A;
   Layout L;
-  // zeroed region
+  // control words and look-back descriptors (cleared once per handle: the
+  // pool may hand back memory that holds another handle's descriptors with
+  // the same epoch numbers), then scratch
   const size_t o_ctr = L.take(sizeof(unsigned) * ep::kCtrWords);
+  const size_t o_desc = L.take(sizeof(unsigned long long) * p.num_tiles * (P + E));
+  h->zero_bytes = L.off;
+  const size_t o_bits = L.take(sizeof(uint32_t) * p.num_tiles * ep::kTileWords * (P + E));
+  const size_t o_wpre = L.take(sizeof(int) * p.num_tiles * ep::kTileWords * (P + E));
   const size_t o_sizes = L.take(sizeof(int) * ep::kSizeWords);
   const size_t o_totals = L.take(sizeof(int) * (P + E));
   const size_t o_ntpe = L.take(sizeof(int) * P * E);
-  const size_t o_desc = L.take(sizeof(unsigned long long) * p.num_tiles * (P + E));
-  h->zero_bytes = L.off;
   // outputs
   const size_t o_ntpr = L.take(sizeof(int) * P * P);
   const size_t o_rpm = L.take(sizeof(int) * P * P);
@@ -132,6 +138,8 @@ size_t layout_handle(ep_handle_s* h, char* base) {
   const size_t total = L.take(0);
   if (base) {
     p.ctr = reinterpret_cast<unsigned*>(base + o_ctr);
+    p.tile_bits = reinterpret_cast<uint32_t*>(base + o_bits);
+    p.tile_wpre = reinterpret_cast<int*>(base + o_wpre);
     p.sizes = reinterpret_cast<int*>(base + o_sizes);
     p.totals = reinterpret_cast<int*>(base + o_totals);
     p.ntpe = reinterpret_cast<int*>(base + o_ntpe);
@@ -157,8 +165,9 @@ ep_status_t enqueue_plan(ep_handle_s* h, const int64_t* topk_idx, cudaStream_t s
   h->dev.topk_idx = topk_idx;
   h->dev.poll_limit = g_poll_limit;
   h->dev.suppress_tile = g_suppress_tile;
-  cudaError_t e = cudaMemsetAsync(h->base, 0, h->zero_bytes, stream);
-  if (e != cudaSuccess) return cuda_status(e);
+  h->epoch = (h->epoch + 1u) & 0x3fffffffu;
+  if (h->epoch == 0u) h->epoch = 1u;  // epoch 0 is what cleared memory holds
+  h->dev.epoch = h->epoch;
   return cuda_status(ep::launch_plan(h->dev, stream));
 }
 
@@ -173,8 +182,11 @@ ep_status_t read_status_word(ep_handle_s* h, cudaStream_t stream, bool clear, in
     if (e != cudaSuccess) return cuda_status(e);
   }
   if (clear && st) {
-    const unsigned zero = 0;
-    e = cudaMemcpy(h->dev.ctr + ep::kCtrStatus, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    // after a timed-out wait the grid-barrier words may be off: reset them too
+    const unsigned zeros[3] = {0u, 0u, 0u};
+    e = (st & ep::kStTimeout)
+            ? cudaMemcpy(h->dev.ctr, zeros, sizeof zeros, cudaMemcpyHostToDevice)
+            : cudaMemcpy(h->dev.ctr + ep::kCtrStatus, zeros, sizeof(unsigned), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_status(e);
   }
   if (st & (ep::kStInvalidId | ep::kStDuplicate)) return EP_ERR_INVALID;
@@ -247,7 +259,8 @@ ep_status_t ep_plan(const int64_t* topk_idx, int64_t S, int P, int K, int E, int
     return cuda_status(e);
   }
   layout_handle(h, static_cast<char*>(h->base));
-  st = enqueue_plan(h, topk_idx, stream);
+  e = cudaMemsetAsync(h->base, 0, h->zero_bytes, stream);
+  st = e == cudaSuccess ? enqueue_plan(h, topk_idx, stream) : cuda_status(e);
   if (st != EP_OK) {
     cudaFreeAsync(h->base, stream);
     delete h;

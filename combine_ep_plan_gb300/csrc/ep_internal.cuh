@@ -17,10 +17,10 @@ constexpr unsigned kStDuplicate = 2u;   // same expert twice in one token row
 constexpr unsigned kStCapacity = 4u;    // an output row at or beyond capacity
 constexpr unsigned kStTimeout = 8u;     // bounded look-back wait gave up
 
-// Counter slots in the zeroed control block.
-constexpr int kCtrTicket = 0;     // tile ticket of the emit kernel
-constexpr int kCtrCountDone = 1;  // CTAs of the count kernel that finished
-constexpr int kCtrStatus = 2;     // device status word
+// Control words (zeroed when a handle is created).
+constexpr int kCtrBarCount = 0;  // grid barrier: CTAs arrived
+constexpr int kCtrBarGen = 1;    // grid barrier: generation
+constexpr int kCtrStatus = 2;    // device status word
 constexpr int kCtrWords = 16;
 
 // Size slots.
@@ -29,7 +29,8 @@ constexpr int kSizeExp = 1;   // N_exp
 constexpr int kSizePad = 2;   // N_pad
 constexpr int kSizeWords = 4;
 
-// Look-back descriptor: high 32 bits = state, low 32 bits = value.
+// Look-back descriptor: high 32 bits = (plan epoch << 2) | state, low 32
+// bits = value.
 constexpr unsigned long long kDescAggregate = 1ull;
 constexpr unsigned long long kDescInclusive = 2ull;
 
@@ -43,13 +44,16 @@ struct PlanDev {
   int ncols;  // P + E: ranks first, then experts
   // input (read during the plan only)
   const int64_t* topk_idx;
-  // zeroed before every plan
-  unsigned* ctr;       // [kCtrWords]
+  // scratch
+  unsigned* ctr;       // [kCtrWords], zeroed once per handle
+  unsigned epoch;      // this plan's epoch (>= 1), tags the descriptors
+  unsigned long long* desc;  // [num_tiles, P+E] look-back descriptors
+  uint32_t* tile_bits; // [num_tiles, kTileWords, P+E] tile bit matrices
+  int* tile_wpre;      // [num_tiles, kTileWords, P+E] exclusive prefix per word
+  // outputs
   int* sizes;          // [kSizeWords]
   int* totals;         // [P+E]: num_recv[d], then expert_counts[e]
   int* ntpe;           // [P,E]  num_tokens_per_expert
-  unsigned long long* desc;  // [num_tiles, P+E] look-back descriptors
-  // outputs
   int* ntpr;           // [P,P]
   int* rpm;            // [P,P]
   int* cpm;            // [P,P,C] [s][d][c]
@@ -70,7 +74,7 @@ struct PlanDev {
 
 // Host-side launchers (defined in the .cu files, called by the C ABI layer).
 cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream);
-size_t plan_emit_smem_bytes(int P, int E, int K);
+size_t plan_smem_bytes(int P, int E, int K);
 
 struct DispatchDev {
   const void* x;          // [T,H] bf16

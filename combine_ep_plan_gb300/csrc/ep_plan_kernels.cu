@@ -1,37 +1,39 @@
-// ep_plan_kernels.cu — the routing plan on sm_103a.
+// ep_plan_kernels.cu — the routing plan on sm_103a, in one cooperative kernel.
 //
-// Three kernels, in stream order:
-//   1. ep_count_kernel: per tile of 256 tokens, a bit matrix in shared memory
-//      with one 32-bit word per (column, warp): column = destination rank d
-//      (deduplicated by the OR) or expert e.  Warp-aggregated updates
-//      (__match_any_sync, one shared atomicOr per distinct key per warp).
-//      Column totals and per-source expert counts go to global memory with one
-//      atomic per non-zero (tile, column).  The last CTA to finish turns the
-//      totals into padded expert offsets, receive-window offsets and padding
-//      offsets.
-//   2. ep_emit_kernel: the same bit matrix, then a single-pass decoupled
-//      look-back scan over tiles, column by column (each descriptor packs its
-//      state and value in one 64-bit word, so no fence pairs are needed), with
-//      a bounded wait.  With the exclusive prefix X of every column it writes
-//      is_token_in_rank, send_head, recv_src_idx, slot, exp_src, the padding
-//      rows, and X at every channel start (the recv_channel_prefix_matrix).
-//   3. ep_prefix_kernel: rank_prefix_matrix, channel_prefix_matrix and
-//      num_tokens_per_rank as differences of X at channel and source starts.
+// Phase 1, one CTA per tile of 256 tokens (CTAs loop if there are more tiles
+// than co-resident CTAs):
+//   - a bit matrix in shared memory, one 32-bit word per (column, warp):
+//     column d < P = "token routed to rank d" (the OR deduplicates the token's
+//     slots that land on one rank), column P+e = "token picked expert e";
+//     warp-aggregated updates (__match_any_sync, one shared atomicOr per
+//     distinct key per warp); invalid and duplicate ids are reported;
+//   - a single-pass decoupled look-back over tiles, column by column: each
+//     descriptor packs (plan epoch, state, value) in one 64-bit word, so a
+//     reader needs no fence pairs and stale descriptors of an earlier plan are
+//     ignored without clearing; eight predecessors per poll; every wait is
+//     bounded;
+//   - the tile's bit matrix and its per-word exclusive prefixes go to global
+//     memory; the last tile writes the column totals.
+// One bounded grid barrier.
+// Phase 2, all CTAs: with X_col(g) = #{g' < g with the bit set in column col}
+// available for any g from two loads, every plan array is computed directly:
+//   send_head[g][d] = X_d(g) (if routed), recv_src_idx, slot[g][k] =
+//   expert_offset[e] + X_e(g), exp_src, padding rows,
+//   recv_channel_prefix[d][s][c] = X_d(start of channel c of source s),
+//   channel_prefix[s][d][c] = X_d(end of channel c) - X_d(s*S),
+//   rank_prefix[s][d] = X_d((s+1)*S), num_tokens_per_rank, and
+//   num_tokens_per_expert[s][e] = X_e((s+1)*S) - X_e(s*S).
 //
-// Definitions followed ("Ascend DeepEP MoE Dispatch Optimization", the
-// dispatch handle table and the notify stage; TileLang tutorial ch. 38
-// "DeepEP-Ascend", §1.3 dedup, §2.2 expanded layout and padding, §3.5
-// deterministic order):
-//   X[g][d]  = #{g' < g : d in dests(g')}             (window row of (g,d))
-//   slot     = expert_offset[e] + #{g' < g : e in idx[g']}
-//   rcpm[d][s][c] = X[s*S + c*chunk][d]                (segment start)
+// Definitions followed: "Ascend DeepEP MoE Dispatch Optimization", the
+// dispatch handle table, the notify stage and the per-channel cursor bases;
+// TileLang tutorial ch. 38 "DeepEP-Ascend", §1.3 dedup, §2.2 expanded layout
+// and padding, §3.5 deterministic order.
 #include "ep_internal.cuh"
 
 namespace ep {
 namespace {
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
-__device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 
 __device__ __forceinline__ unsigned long long ld_desc(const unsigned long long* p) {
   unsigned long long v;
@@ -43,48 +45,41 @@ __device__ __forceinline__ void st_desc(unsigned long long* p, unsigned long lon
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// Bits set in word-columns [0, i) of one column of the tile bit matrix
-// (layout bits[w * ncols + col]).
-__device__ __forceinline__ int prefix_in_tile(const uint32_t* bits, int ncols, int col, int i) {
-  int w = i >> 5;
-  int n = 0;
-#pragma unroll
-  for (int j = 0; j < kTileWords; ++j)
-    if (j < w) n += __popc(bits[j * ncols + col]);
-  uint32_t lt = (i & 31) ? (0xffffffffu >> (32 - (i & 31))) : 0u;
-  if (w < kTileWords) n += __popc(bits[w * ncols + col] & lt);
-  return n;
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
-// Bits set in tokens [lo, hi) of one column.
-__device__ __forceinline__ int count_range(const uint32_t* bits, int ncols, int col, int lo, int hi) {
-  return prefix_in_tile(bits, ncols, col, hi) - prefix_in_tile(bits, ncols, col, lo);
+__device__ __forceinline__ unsigned long long pack_desc(unsigned epoch, unsigned long long state, int value) {
+  return (static_cast<unsigned long long>((epoch << 2) | static_cast<unsigned>(state)) << 32) |
+         static_cast<unsigned>(value);
 }
+
+// Lanes below l within a word.
+__device__ __forceinline__ uint32_t lanes_below(int l) { return l ? (0xffffffffu >> (32 - l)) : 0u; }
 
 // Loads this tile's expert ids into shared memory (coalesced), checking them.
-__device__ __forceinline__ void load_tile_ids(const PlanDev& p, int64_t t0, int* ids, bool report) {
+__device__ __forceinline__ void load_tile_ids(const PlanDev& p, int64_t t0, int* ids) {
   const int64_t base = t0 * p.K;
   const int64_t end = p.T * p.K;
   for (int i = threadIdx.x; i < kTile * p.K; i += blockDim.x) {
     int e = -1;
     if (base + i < end) {
       long long v = p.topk_idx[base + i];
-      if (v >= 0 && v < p.E) {
+      if (v >= 0 && v < p.E)
         e = static_cast<int>(v);
-      } else if (v != -1 && report) {
+      else if (v != -1)
         atomicOr(&p.ctr[kCtrStatus], kStInvalidId);
-      }
     }
     ids[i] = e;
   }
 }
 
-// Builds the tile bit matrix from the ids (shared memory must be zeroed).
-// Column d < P: token routed to rank d (OR deduplicates); column P+e: token
-// picked expert e.  A duplicate expert in one row shows up as a bit that is
-// already set when the leader ORs its lane mask.
-__device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids, uint32_t* bits,
-                                                bool report) {
+// Builds the tile bit matrix (layout bits[w * ncols + col], zeroed before).
+// A duplicate expert in one row shows up as a bit already set when the
+// leader ORs its lane mask.
+__device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids, uint32_t* bits) {
   const int lane = threadIdx.x & 31;
   const int w = threadIdx.x >> 5;
   for (int k = 0; k < p.K; ++k) {
@@ -92,7 +87,7 @@ __device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids
     const unsigned me = __match_any_sync(0xffffffffu, e);
     if (e >= 0 && lane == __ffs(me) - 1) {
       unsigned old = atomicOr(&bits[w * p.ncols + p.P + e], me);
-      if ((old & me) && report) atomicOr(&p.ctr[kCtrStatus], kStDuplicate);
+      if (old & me) atomicOr(&p.ctr[kCtrStatus], kStDuplicate);
     }
     const int d = e >= 0 ? e / p.El : -1;
     const unsigned md = __match_any_sync(0xffffffffu, d);
@@ -100,7 +95,86 @@ __device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids
   }
 }
 
-// Inclusive-to-exclusive scan of n ints in place, one CTA; returns the total.
+// Exclusive prefix of one column over all earlier tiles: walk back through
+// predecessors eight at a time, adding aggregates until an inclusive prefix
+// is found.  A descriptor of another epoch counts as not yet published.
+__device__ int lookback(const PlanDev& p, int tile, int col, bool* timed_out) {
+  constexpr int kWindow = 8;
+  int sum = 0;
+  int j = tile - 1;
+  long long polls = 0;
+  while (j >= 0) {
+    unsigned long long v[kWindow];
+#pragma unroll
+    for (int u = 0; u < kWindow; ++u)
+      v[u] = (j - u >= 0) ? ld_desc(&p.desc[static_cast<int64_t>(j - u) * p.ncols + col]) : 0ull;
+#pragma unroll
+    for (int u = 0; u < kWindow; ++u) {
+      if (j - u < 0) break;
+      unsigned long long d = v[u];
+      unsigned ns = 32;
+      while (static_cast<unsigned>(d >> 34) != p.epoch || ((d >> 32) & 3ull) == 0ull) {
+        if (++polls > p.poll_limit) {
+          *timed_out = true;
+          return sum;  // give up; the plan is flagged invalid
+        }
+        __nanosleep(ns);
+        if (ns < 1024) ns <<= 1;
+        d = ld_desc(&p.desc[static_cast<int64_t>(j - u) * p.ncols + col]);
+      }
+      sum += static_cast<int>(static_cast<unsigned>(d));
+      if (((d >> 32) & 3ull) == kDescInclusive) return sum;
+    }
+    j -= kWindow;
+  }
+  return sum;
+}
+
+// Bounded grid-wide barrier for a cooperative launch: the last CTA to arrive
+// resets the count and bumps the generation the others wait on.
+__device__ bool grid_sync(const PlanDev& p) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned* count = p.ctr + kCtrBarCount;
+    unsigned* gen = p.ctr + kCtrBarGen;
+    const unsigned g0 = ld_acquire(gen);
+    __threadfence();
+    const unsigned arrived = atomicAdd(count, 1u) + 1u;
+    int ok = 1;
+    if (arrived == gridDim.x) {
+      atomicExch(count, 0u);
+      __threadfence();
+      atomicAdd(gen, 1u);
+    } else {
+      long long polls = 0;
+      unsigned ns = 32;
+      while (ld_acquire(gen) == g0) {
+        if (++polls > p.poll_limit) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(ns);
+        if (ns < 1024) ns <<= 1;
+      }
+    }
+    __threadfence();
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+
+// X_col(g): bits set in column col for tokens before g (g in [0, T]).
+__device__ __forceinline__ int x_at(const PlanDev& p, int col, int64_t g) {
+  if (g >= p.T) return __ldcg(&p.totals[col]);
+  const int64_t t = g / kTile;
+  const int gl = static_cast<int>(g - t * kTile);
+  const int64_t at = (t * kTileWords + (gl >> 5)) * p.ncols + col;
+  return __ldcg(&p.tile_wpre[at]) + __popc(__ldcg(&p.tile_bits[at]) & lanes_below(gl & 31));
+}
+
+// Exclusive scan of n ints in shared memory, one CTA; returns the total.
 __device__ int block_exclusive_scan(int* a, int n, int* scratch /* blockDim.x */) {
   const int nt = blockDim.x;
   const int per = (n + nt - 1) / nt;
@@ -128,305 +202,199 @@ __device__ int block_exclusive_scan(int* a, int n, int* scratch /* blockDim.x */
   return total;
 }
 
-__global__ void __launch_bounds__(kTile) ep_count_kernel(PlanDev p) {
+__global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   extern __shared__ __align__(16) uint32_t smem[];
-  uint32_t* bits = smem;                                       // [kTileWords * ncols]
-  int* ids = reinterpret_cast<int*>(bits + kTileWords * p.ncols);  // [kTile * K]
   __shared__ int scan_scratch[kTile];
-  __shared__ bool is_last;
 
-  const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTile;
-  const int rows = static_cast<int>(min64(kTile, p.T - t0));
-  for (int i = threadIdx.x; i < kTileWords * p.ncols; i += blockDim.x) bits[i] = 0u;
-  load_tile_ids(p, t0, ids, true);
-  __syncthreads();
-  build_tile_bits(p, ids, bits, true);
-  __syncthreads();
+  // ---------------- phase 1: tiles ----------------
+  uint32_t* bits = smem;                                           // [kTileWords * ncols]
+  int* ids = reinterpret_cast<int*>(bits + kTileWords * p.ncols);  // [kTile * K]
+  bool timed_out = false;
+  for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    const int64_t t0 = static_cast<int64_t>(tile) * kTile;
+    for (int i = threadIdx.x; i < kTileWords * p.ncols; i += blockDim.x) bits[i] = 0u;
+    load_tile_ids(p, t0, ids);
+    __syncthreads();
+    build_tile_bits(p, ids, bits);
+    __syncthreads();
+    uint32_t* g_bits = p.tile_bits + static_cast<int64_t>(tile) * kTileWords * p.ncols;
+    int* g_wpre = p.tile_wpre + static_cast<int64_t>(tile) * kTileWords * p.ncols;
+    for (int i = threadIdx.x; i < kTileWords * p.ncols; i += blockDim.x) g_bits[i] = bits[i];
 
-  // Column totals and per-source expert counts (one atomic per non-zero pair).
-  const int64_t s_first = t0 / p.S;
-  const int64_t s_last = (t0 + rows - 1) / p.S;
-  for (int col = threadIdx.x; col < p.ncols; col += blockDim.x) {
-    int n = 0;
+    const bool publish = tile != p.suppress_tile;
+    unsigned long long* my_desc = p.desc + static_cast<int64_t>(tile) * p.ncols;
+    // aggregates first (all columns), so successors never wait on our look-back
+    for (int col = threadIdx.x; col < p.ncols; col += blockDim.x) {
+      int n = 0;
 #pragma unroll
-    for (int j = 0; j < kTileWords; ++j) n += __popc(bits[j * p.ncols + col]);
-    if (n == 0) continue;
-    atomicAdd(&p.totals[col], n);
-    if (col >= p.P) {
-      const int e = col - p.P;
-      if (s_first == s_last) {
-        atomicAdd(&p.ntpe[s_first * p.E + e], n);
-      } else {
-        for (int64_t s = s_first; s <= s_last; ++s) {
-          int lo = static_cast<int>(max64(s * p.S, t0) - t0);
-          int hi = static_cast<int>(min64((s + 1) * p.S, t0 + rows) - t0);
-          int m = count_range(bits, p.ncols, col, lo, hi);
-          if (m) atomicAdd(&p.ntpe[s * p.E + e], m);
-        }
-      }
+      for (int j = 0; j < kTileWords; ++j) n += __popc(bits[j * p.ncols + col]);
+      if (publish) st_desc(&my_desc[col], pack_desc(p.epoch, tile == 0 ? kDescInclusive : kDescAggregate, n));
     }
+    for (int col = threadIdx.x; col < p.ncols; col += blockDim.x) {
+      int run = tile > 0 ? lookback(p, tile, col, &timed_out) : 0;
+      int n = 0;
+#pragma unroll
+      for (int j = 0; j < kTileWords; ++j) {
+        g_wpre[j * p.ncols + col] = run + n;
+        n += __popc(bits[j * p.ncols + col]);
+      }
+      if (publish && tile > 0) st_desc(&my_desc[col], pack_desc(p.epoch, kDescInclusive, run + n));
+      if (tile == p.num_tiles - 1) p.totals[col] = run + n;
+    }
+    __syncthreads();  // before the next tile reuses shared memory
+  }
+  if (timed_out) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
+
+  if (!grid_sync(p)) {
+    if (threadIdx.x == 0) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
+    return;
   }
 
-  // The last CTA derives the offsets from the totals.
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) is_last = atomicAdd(&p.ctr[kCtrCountDone], 1u) == gridDim.x - 1;
-  __syncthreads();
-  if (!is_last) return;
-  __threadfence();
-
-  // Reuse the bit-matrix space: [E+1] padded sizes, [E+1] pads, [P+1] receives.
-  int* padded = reinterpret_cast<int*>(smem);
-  int* pads = padded + (p.E + 1);
-  int* recv = pads + (p.E + 1);
+  // ---------------- phase 2: every plan array, all CTAs ----------------
+  int* exp_off = reinterpret_cast<int*>(smem);  // [E+1]
+  int* pad_off = exp_off + (p.E + 1);           // [E+1]
+  int* recv_off = pad_off + (p.E + 1);          // [P+1]
   for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
     const int n = __ldcg(&p.totals[p.P + e]);
     const int v = (n + p.A - 1) / p.A * p.A;
-    padded[e] = v;
-    pads[e] = v - n;
+    exp_off[e] = v;
+    pad_off[e] = v - n;
   }
-  for (int d = threadIdx.x; d < p.P; d += blockDim.x) recv[d] = __ldcg(&p.totals[d]);
+  for (int d = threadIdx.x; d < p.P; d += blockDim.x) recv_off[d] = __ldcg(&p.totals[d]);
   __syncthreads();
-  const int n_exp = block_exclusive_scan(padded, p.E, scan_scratch);
-  const int n_pad = block_exclusive_scan(pads, p.E, scan_scratch);
-  const int n_recv = block_exclusive_scan(recv, p.P, scan_scratch);
-  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
-    p.exp_off[e] = padded[e];
-    p.pad_off[e] = pads[e];
-  }
-  for (int d = threadIdx.x; d < p.P; d += blockDim.x) p.recv_off[d] = recv[d];
+  const int n_exp = block_exclusive_scan(exp_off, p.E, scan_scratch);
+  const int n_pad = block_exclusive_scan(pad_off, p.E, scan_scratch);
+  const int n_recv = block_exclusive_scan(recv_off, p.P, scan_scratch);
   if (threadIdx.x == 0) {
-    p.exp_off[p.E] = n_exp;
-    p.pad_off[p.E] = n_pad;
-    p.recv_off[p.P] = n_recv;
-    p.sizes[kSizeRecv] = n_recv;
-    p.sizes[kSizeExp] = n_exp;
-    p.sizes[kSizePad] = n_pad;
+    exp_off[p.E] = n_exp;
+    pad_off[p.E] = n_pad;
+    recv_off[p.P] = n_recv;
   }
-}
-
-// Exclusive prefix of one column over all earlier tiles, by decoupled
-// look-back: walk back through predecessors eight at a time, adding
-// aggregates until an inclusive prefix is found.  Every poll is bounded.
-__device__ int lookback(const PlanDev& p, int tile, int col, bool* timed_out) {
-  constexpr int kWindow = 8;
-  int sum = 0;
-  int j = tile - 1;
-  long long polls = 0;
-  while (j >= 0) {
-    unsigned long long v[kWindow];
-#pragma unroll
-    for (int u = 0; u < kWindow; ++u)
-      v[u] = (j - u >= 0) ? ld_desc(&p.desc[static_cast<int64_t>(j - u) * p.ncols + col]) : 0ull;
-#pragma unroll
-    for (int u = 0; u < kWindow; ++u) {
-      if (j - u < 0) break;
-      unsigned long long d = v[u];
-      unsigned ns = 32;
-      while ((d >> 32) == 0ull) {
-        if (++polls > p.poll_limit) {
-          *timed_out = true;
-          return sum;  // give up; the result is flagged invalid
-        }
-        __nanosleep(ns);
-        if (ns < 1024) ns <<= 1;
-        d = ld_desc(&p.desc[static_cast<int64_t>(j - u) * p.ncols + col]);
-      }
-      sum += static_cast<int>(static_cast<unsigned>(d));
-      if ((d >> 32) == kDescInclusive) return sum;
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+      p.exp_off[i] = exp_off[i];
+      p.pad_off[i] = pad_off[i];
     }
-    j -= kWindow;
-  }
-  return sum;
-}
-
-__global__ void __launch_bounds__(kTile) ep_emit_kernel(PlanDev p) {
-  extern __shared__ __align__(16) uint32_t smem[];
-  uint32_t* bits = smem;                                           // [kTileWords * ncols]
-  int* excl = reinterpret_cast<int*>(bits + kTileWords * p.ncols);  // [ncols]
-  int* ids = excl + p.ncols;                                       // [kTile * K]
-  int* recv_off = ids + kTile * p.K;                               // [P+1]
-  int* exp_off = recv_off + (p.P + 1);                             // [E+1]
-  __shared__ int s_tile;
-  __shared__ int s_timeout;
-
-  if (threadIdx.x == 0) {
-    s_tile = static_cast<int>(atomicAdd(&p.ctr[kCtrTicket], 1u));
-    s_timeout = 0;
-  }
-  for (int i = threadIdx.x; i < kTileWords * p.ncols; i += blockDim.x) bits[i] = 0u;
-  for (int i = threadIdx.x; i <= p.P; i += blockDim.x) recv_off[i] = p.recv_off[i];
-  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) exp_off[i] = p.exp_off[i];
-  __syncthreads();
-  const int tile = s_tile;
-  const int64_t t0 = static_cast<int64_t>(tile) * kTile;
-  const int rows = static_cast<int>(min64(kTile, p.T - t0));
-  load_tile_ids(p, t0, ids, false);
-  __syncthreads();
-  build_tile_bits(p, ids, bits, false);
-  __syncthreads();
-
-  // Publish this tile's aggregate (tile 0: its inclusive prefix) per column.
-  const bool publish = tile != p.suppress_tile;
-  unsigned long long* my_desc = p.desc + static_cast<int64_t>(tile) * p.ncols;
-  for (int col = threadIdx.x; col < p.ncols; col += blockDim.x) {
-    int n = 0;
-#pragma unroll
-    for (int j = 0; j < kTileWords; ++j) n += __popc(bits[j * p.ncols + col]);
-    excl[col] = n;
-    if (publish)
-      st_desc(&my_desc[col], ((tile == 0 ? kDescInclusive : kDescAggregate) << 32) |
-                                 static_cast<unsigned>(n));
-  }
-  // Look back, then publish the inclusive prefix.
-  if (tile > 0) {
-    bool timed_out = false;
-    for (int col = threadIdx.x; col < p.ncols; col += blockDim.x) {
-      const int n = excl[col];
-      const int pre = lookback(p, tile, col, &timed_out);
-      excl[col] = pre;
-      if (publish) st_desc(&my_desc[col], (kDescInclusive << 32) | static_cast<unsigned>(pre + n));
-    }
-    if (timed_out) s_timeout = 1;
-  } else {
-    for (int col = threadIdx.x; col < p.ncols; col += blockDim.x) excl[col] = 0;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && s_timeout) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
-
-  // slot and exp_src, one thread per token.
-  if (threadIdx.x < rows) {
-    const int64_t g = t0 + threadIdx.x;
-    for (int k = 0; k < p.K; ++k) {
-      const int e = ids[threadIdx.x * p.K + k];
-      int r = -1;
-      if (e >= 0) {
-        const int col = p.P + e;
-        r = exp_off[e] + excl[col] + prefix_in_tile(bits, p.ncols, col, threadIdx.x);
-        p.exp_src[r] = static_cast<int>(g);
-      }
-      p.slot[g * p.K + k] = r;
+    for (int i = threadIdx.x; i <= p.P; i += blockDim.x) p.recv_off[i] = recv_off[i];
+    if (threadIdx.x == 0) {
+      p.sizes[kSizeRecv] = n_recv;
+      p.sizes[kSizeExp] = n_exp;
+      p.sizes[kSizePad] = n_pad;
     }
   }
 
-  // Dense [rows, P] outputs: is_token_in_rank, send_head, and recv_src_idx.
-  const int dense = rows * p.P;
-  for (int i = threadIdx.x; i < dense; i += blockDim.x) {
-    const int gl = i / p.P;
-    const int d = i - gl * p.P;
-    const uint32_t word = bits[(gl >> 5) * p.ncols + d];
+  const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+
+  // slot and exp_src
+  for (int64_t i = gtid; i < p.T * p.K; i += nthr) {
+    const int64_t g = i / p.K;
+    const long long v = p.topk_idx[i];
+    int r = -1;
+    if (v >= 0 && v < p.E) {
+      const int e = static_cast<int>(v);
+      r = exp_off[e] + x_at(p, p.P + e, g);
+      p.exp_src[r] = static_cast<int>(g);
+    }
+    p.slot[i] = r;
+  }
+
+  // dense [T,P]: is_token_in_rank, send_head, and recv_src_idx
+  for (int64_t i = gtid; i < p.T * p.P; i += nthr) {
+    const int64_t g = i / p.P;
+    const int d = static_cast<int>(i - g * p.P);
+    const int64_t t = g / kTile;
+    const int gl = static_cast<int>(g - t * kTile);
+    const int64_t at = (t * kTileWords + (gl >> 5)) * p.ncols + d;
+    const uint32_t word = __ldcg(&p.tile_bits[at]);
     const int bit = (word >> (gl & 31)) & 1;
-    const int64_t g = t0 + gl;
     int pos = -1;
     if (bit) {
-      pos = excl[d] + prefix_in_tile(bits, p.ncols, d, gl);
+      pos = __ldcg(&p.tile_wpre[at]) + __popc(word & lanes_below(gl & 31));
       p.recv_src_idx[recv_off[d] + pos] = static_cast<int>(g % p.S);
     }
-    p.in_rank[t0 * p.P + i] = static_cast<unsigned char>(bit);
-    p.send_head[t0 * p.P + i] = pos;
+    p.in_rank[i] = static_cast<unsigned char>(bit);
+    p.send_head[i] = pos;
   }
 
-  // X at every channel start inside this tile: the segment starts of the
-  // recv_channel_prefix_matrix.
-  const int64_t s_first = t0 / p.S;
-  const int64_t s_last = (t0 + rows - 1) / p.S;
-  for (int64_t s = s_first; s <= s_last; ++s) {
+  // prefix matrices, one (s, d, c) per thread; layout of i is [s][d][c]
+  for (int64_t i = gtid; i < static_cast<int64_t>(p.P) * p.P * p.C; i += nthr) {
+    const int c = static_cast<int>(i % p.C);
+    const int64_t sd = i / p.C;
+    const int d = static_cast<int>(sd % p.P);
+    const int64_t s = sd / p.P;
     const int64_t src0 = s * p.S;
-    // channels c with start src0 + c*chunk in [t0, t0 + rows) and c*chunk < S
-    int64_t c_lo = t0 > src0 ? (t0 - src0 + p.chunk - 1) / p.chunk : 0;
-    int64_t c_hi = (t0 + rows - 1 - src0) / p.chunk;  // inclusive
-    c_hi = min64(c_hi, p.C - 1);
-    c_hi = min64(c_hi, (p.S - 1) / p.chunk);
-    if (c_hi < c_lo) continue;
-    const int nstart = static_cast<int>(c_hi - c_lo + 1);
-    for (int i = threadIdx.x; i < nstart * p.P; i += blockDim.x) {
-      const int ci = i / p.P;
-      const int d = i - ci * p.P;
-      const int64_t c = c_lo + ci;
-      const int gl = static_cast<int>(src0 + c * p.chunk - t0);
-      p.rcpm[(static_cast<int64_t>(d) * p.P + s) * p.C + c] =
-          excl[d] + prefix_in_tile(bits, p.ncols, d, gl);
+    const int64_t lo = src0 + min64(p.S, static_cast<int64_t>(c) * p.chunk);
+    const int64_t hi = src0 + min64(p.S, static_cast<int64_t>(c + 1) * p.chunk);
+    const int x0 = x_at(p, d, src0);
+    p.rcpm[(static_cast<int64_t>(d) * p.P + s) * p.C + c] = x_at(p, d, lo);
+    p.cpm[i] = x_at(p, d, hi) - x0;
+    if (c == 0) {
+      const int x1 = x_at(p, d, src0 + p.S);
+      p.rpm[s * p.P + d] = x1;
+      p.ntpr[s * p.P + d] = x1 - x0;
     }
   }
 
-  // Padding rows of the expanded layout, spread over the tiles.
-  const int n_pad = p.sizes[kSizePad];
-  for (int64_t i = static_cast<int64_t>(tile) * kTile + threadIdx.x; i < n_pad;
-       i += static_cast<int64_t>(p.num_tiles) * kTile) {
-    int lo = 0, hi = p.E;  // find e with pad_off[e] <= i < pad_off[e+1]
+  // per-source expert counts
+  for (int64_t i = gtid; i < static_cast<int64_t>(p.P) * p.E; i += nthr) {
+    const int64_t s = i / p.E;
+    const int e = static_cast<int>(i - s * p.E);
+    p.ntpe[i] = x_at(p, p.P + e, (s + 1) * p.S) - x_at(p, p.P + e, s * p.S);
+  }
+
+  // padding rows of the expanded layout
+  for (int64_t i = gtid; i < n_pad; i += nthr) {
+    int lo = 0, hi = p.E;  // e with pad_off[e] <= i < pad_off[e+1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (p.pad_off[mid] <= i) lo = mid; else hi = mid;
+      if (pad_off[mid] <= i) lo = mid; else hi = mid;
     }
     const int e = lo;
-    const int row = exp_off[e] + p.totals[p.P + e] + static_cast<int>(i - p.pad_off[e]);
+    const int n_e = (exp_off[e + 1] - exp_off[e]) - (pad_off[e + 1] - pad_off[e]);
+    const int row = exp_off[e] + n_e + static_cast<int>(i - pad_off[e]);
     p.pad_rows[i] = row;
     p.exp_src[row] = -1;
   }
 }
 
-__global__ void ep_prefix_kernel(PlanDev p) {
-  const int64_t total = static_cast<int64_t>(p.P) * p.P * p.C;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= total) return;
-  const int c = static_cast<int>(i % p.C);
-  const int64_t sd = i / p.C;
-  const int d = static_cast<int>(sd % p.P);
-  const int s = static_cast<int>(sd / p.P);
-  // X at the start of source s2 (s2 == P: the end of the last source).
-  auto x_src = [&](int s2) -> int {
-    return s2 < p.P ? p.rcpm[(static_cast<int64_t>(d) * p.P + s2) * p.C] : p.totals[d];
-  };
-  auto channel_live = [&](int c2) { return c2 < p.C && static_cast<int64_t>(c2) * p.chunk < p.S; };
-  const int x0 = x_src(s);
-  const int x_end = x_src(s + 1);
-  const int x_next = channel_live(c + 1) ? p.rcpm[(static_cast<int64_t>(d) * p.P + s) * p.C + c + 1] : x_end;
-  p.cpm[i] = x_next - x0;
-  if (!channel_live(c)) p.rcpm[(static_cast<int64_t>(d) * p.P + s) * p.C + c] = x_end;
-  if (c == 0) {
-    p.rpm[static_cast<int64_t>(s) * p.P + d] = x_end;
-    p.ntpr[static_cast<int64_t>(s) * p.P + d] = x_end - x0;
-  }
-}
-
-size_t count_smem_bytes(const PlanDev& p) {
-  size_t a = sizeof(uint32_t) * kTileWords * p.ncols + sizeof(int) * kTile * p.K;
-  size_t b = sizeof(int) * (2 * (p.E + 1) + (p.P + 1));  // finalize reuse
-  return a > b ? a : b;
-}
-
 }  // namespace
 
-size_t plan_emit_smem_bytes(int P, int E, int K) {
-  const int ncols = P + E;
-  return sizeof(uint32_t) * kTileWords * ncols + sizeof(int) * ncols + sizeof(int) * kTile * K +
-         sizeof(int) * (P + 1 + E + 1);
+size_t plan_smem_bytes(int P, int E, int K) {
+  const size_t phase1 = sizeof(uint32_t) * kTileWords * (P + E) + sizeof(int) * kTile * K;
+  const size_t phase2 = sizeof(int) * (2 * (E + 1) + (P + 1));
+  return phase1 > phase2 ? phase1 : phase2;
+}
+
+int plan_grid(const PlanDev& p) {
+  const size_t smem = plan_smem_bytes(p.P, p.E, p.K);
+  static size_t cached_smem = ~static_cast<size_t>(0);
+  static int cached_grid = 0;
+  if (smem == cached_smem) return cached_grid;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_plan_kernel, kTile, smem) != cudaSuccess ||
+      per_sm < 1)
+    return 0;
+  if (per_sm > 4) per_sm = 4;
+  cached_grid = per_sm * num_sms();
+  cached_smem = smem;
+  return cached_grid;
 }
 
 cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream) {
-  const size_t count_smem = count_smem_bytes(p);
-  const size_t emit_smem = plan_emit_smem_bytes(p.P, p.E, p.K);
-  cudaError_t err;
-  if (count_smem > 48 * 1024) {
-    err = cudaFuncSetAttribute(ep_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(count_smem));
+  const size_t smem = plan_smem_bytes(p.P, p.E, p.K);
+  if (smem > 48 * 1024) {
+    cudaError_t err = cudaFuncSetAttribute(ep_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
     if (err != cudaSuccess) return err;
   }
-  if (emit_smem > 48 * 1024) {
-    err = cudaFuncSetAttribute(ep_emit_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(emit_smem));
-    if (err != cudaSuccess) return err;
-  }
-  ep_count_kernel<<<p.num_tiles, kTile, count_smem, stream>>>(p);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  ep_emit_kernel<<<p.num_tiles, kTile, emit_smem, stream>>>(p);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
-  const int64_t total = static_cast<int64_t>(p.P) * p.P * p.C;
-  const int threads = 256;
-  ep_prefix_kernel<<<static_cast<unsigned>((total + threads - 1) / threads), threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  const int grid = plan_grid(p);
+  if (grid < 1) return cudaErrorInvalidConfiguration;
+  PlanDev arg = p;
+  void* args[] = {&arg};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(ep_plan_kernel), dim3(grid), dim3(kTile),
+                                     args, smem, stream);
 }
 
 }  // namespace ep

@@ -75,15 +75,19 @@ extern "C" ep_status_t ep_plan_static_scratch(const int64_t* topk_idx, int64_t S
       !aligned4(out->slot) || !aligned4(out->exp_src) || !aligned4(out->pad_rows) || !aligned4(out->info))
     return EP_ERR_INVALID;
 
-  // Scratch layout: control words, sizes, column totals, look-back descriptors.
+  // Scratch layout: control words, look-back descriptors, tile bit matrices
+  // and word prefixes, sizes, column totals, padding offsets.
   const int ncols = P + E;
   const int num_tiles = static_cast<int>((T + ep::kTile - 1) / ep::kTile);
+  const size_t tile_words = static_cast<size_t>(num_tiles) * ep::kTileWords * ncols;
   const size_t o_ctr = 0;
-  const size_t o_sizes = round256(o_ctr + sizeof(unsigned) * ep::kCtrWords);
-  const size_t o_totals = round256(o_sizes + sizeof(int) * ep::kSizeWords);
-  const size_t o_desc = round256(o_totals + sizeof(int) * ncols);
+  const size_t o_desc = round256(o_ctr + sizeof(unsigned) * ep::kCtrWords);
   const size_t cleared = o_desc + sizeof(unsigned long long) * static_cast<size_t>(num_tiles) * ncols;
-  const size_t o_padoff = round256(cleared);
+  const size_t o_bits = round256(cleared);
+  const size_t o_wpre = round256(o_bits + sizeof(uint32_t) * tile_words);
+  const size_t o_sizes = round256(o_wpre + sizeof(int) * tile_words);
+  const size_t o_totals = round256(o_sizes + sizeof(int) * ep::kSizeWords);
+  const size_t o_padoff = round256(o_totals + sizeof(int) * ncols);
   if (o_padoff + sizeof(int) * (E + 1) > EP_STATIC_SCRATCH_BYTES) return EP_ERR_CAPACITY;
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -93,11 +97,9 @@ extern "C" ep_status_t ep_plan_static_scratch(const int64_t* topk_idx, int64_t S
   char* base = static_cast<char*>(base_v);
 
   // Every call shares the scratch and finds the last call's contents in it:
-  // clear the part this plan accumulates into, and the caller's per-source
-  // expert counts, which the count kernel accumulates too.
+  // clear the control words and the look-back descriptors (the plan runs with
+  // epoch 1, which cleared descriptors never carry); the rest is overwritten.
   e = cudaMemsetAsync(base, 0, cleared, stream);
-  if (e == cudaSuccess)
-    e = cudaMemsetAsync(out->num_tokens_per_expert, 0, sizeof(int) * static_cast<size_t>(P) * E, stream);
   if (e != cudaSuccess) return to_status(e);
 
   ep::PlanDev p{};
@@ -114,9 +116,12 @@ extern "C" ep_status_t ep_plan_static_scratch(const int64_t* topk_idx, int64_t S
   p.ncols = ncols;
   p.topk_idx = topk_idx;
   p.ctr = reinterpret_cast<unsigned*>(base + o_ctr);
+  p.epoch = 1u;
+  p.desc = reinterpret_cast<unsigned long long*>(base + o_desc);
+  p.tile_bits = reinterpret_cast<uint32_t*>(base + o_bits);
+  p.tile_wpre = reinterpret_cast<int*>(base + o_wpre);
   p.sizes = reinterpret_cast<int*>(base + o_sizes);
   p.totals = reinterpret_cast<int*>(base + o_totals);
-  p.desc = reinterpret_cast<unsigned long long*>(base + o_desc);
   p.ntpe = out->num_tokens_per_expert;
   p.ntpr = out->num_tokens_per_rank;
   p.rpm = out->rank_prefix;

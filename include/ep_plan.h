@@ -265,10 +265,11 @@ ep_status_t ep_handle_destroy(ep_handle_t handle, ep_stream_t stream);
  *   call's contents; each call clears what it needs.  Calls whose work
  *   overlaps on the GPU (other streams, other threads) race on the scratch:
  *   order them.
- * - Scratch need: about 8*ceil(T/256)*(P+E) + 4*(P+2E) + 1 KB bytes; a plan
- *   that would need more than EP_STATIC_SCRATCH_BYTES returns
- *   EP_ERR_CAPACITY before anything is enqueued (16384 tokens with P+E = 384
- *   need about 0.2 MB; the limit allows e.g. 65536 tokens with P+E = 1900).
+ * - Scratch need: about 0.28*T*(P+E) + 4*(P+2E) + 2 KB bytes (look-back
+ *   descriptors, tile bit matrices and their word prefixes); a plan that
+ *   would need more than EP_STATIC_SCRATCH_BYTES returns EP_ERR_CAPACITY
+ *   before anything is enqueued (16384 tokens with P+E = 384 need about
+ *   1.8 MB; 65536 tokens fit with P+E up to about 220).
  * - Arguments and shape limits are those of ep_plan; out and all its pointers
  *   must be non-NULL device pointers, 4-byte aligned except the uint8 array.
  *   out->info receives {N_recv, N_exp, N_pad, device status bits}; status

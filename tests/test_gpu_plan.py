@@ -143,3 +143,15 @@ def test_worst_expanded_rows_bounds_exact_size():
         idx, _ = draw_topk(w)
         h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
         assert h.sizes()[0] <= ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
+
+
+def test_new_handle_on_reused_pool_memory():
+    """A handle made right after another one was destroyed gets the same pool
+    memory back, stale look-back descriptors included: its plan must ignore
+    them."""
+    w = WORKLOADS["bf16"].scaled(S=300)
+    for seed in range(4):
+        idx, _ = draw_topk(w, seed=100 + seed)
+        h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
+        assert_plan_equal(gpu_plan_arrays(h), oracle.plan(idx, w.S, w.P, w.E, w.A))
+        h.destroy()
