@@ -28,6 +28,7 @@
 // dispatch handle table, the notify stage and the per-channel cursor bases;
 // TileLang tutorial ch. 38 "DeepEP-Ascend", §1.3 dedup, §2.2 expanded layout
 // and padding, §3.5 deterministic order.
+#include "ep_plan.h"
 #include "ep_internal.cuh"
 
 namespace ep {
@@ -60,19 +61,28 @@ __device__ __forceinline__ unsigned long long pack_desc(unsigned epoch, unsigned
 __device__ __forceinline__ uint32_t lanes_below(int l) { return l ? (0xffffffffu >> (32 - l)) : 0u; }
 
 // Loads this tile's expert ids into shared memory (coalesced), checking them.
+// All of a thread's loads are issued before any is used.
 __device__ __forceinline__ void load_tile_ids(const PlanDev& p, int64_t t0, int* ids) {
   const int64_t base = t0 * p.K;
   const int64_t end = p.T * p.K;
-  for (int i = threadIdx.x; i < kTile * p.K; i += blockDim.x) {
-    int e = -1;
-    if (base + i < end) {
-      long long v = p.topk_idx[base + i];
-      if (v >= 0 && v < p.E)
-        e = static_cast<int>(v);
-      else if (v != -1)
+  const int n = kTile * p.K;  // <= kTile * EP_MAX_TOPK
+  long long v[EP_MAX_TOPK];
+#pragma unroll
+  for (int u = 0; u < EP_MAX_TOPK; ++u) {
+    const int i = threadIdx.x + u * kTile;
+    v[u] = (i < n && base + i < end) ? p.topk_idx[base + i] : -1ll;
+  }
+#pragma unroll
+  for (int u = 0; u < EP_MAX_TOPK; ++u) {
+    const int i = threadIdx.x + u * kTile;
+    if (i < n) {
+      int e = -1;
+      if (v[u] >= 0 && v[u] < p.E)
+        e = static_cast<int>(v[u]);
+      else if (v[u] != -1)
         atomicOr(&p.ctr[kCtrStatus], kStInvalidId);
+      ids[i] = e;
     }
-    ids[i] = e;
   }
 }
 
@@ -96,10 +106,10 @@ __device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids
 }
 
 // Exclusive prefix of one column over all earlier tiles: walk back through
-// predecessors eight at a time, adding aggregates until an inclusive prefix
+// predecessors sixteen at a time, adding aggregates until an inclusive prefix
 // is found.  A descriptor of another epoch counts as not yet published.
 __device__ int lookback(const PlanDev& p, int tile, int col, bool* timed_out) {
-  constexpr int kWindow = 8;
+  constexpr int kWindow = 16;
   int sum = 0;
   int j = tile - 1;
   long long polls = 0;
@@ -119,7 +129,7 @@ __device__ int lookback(const PlanDev& p, int tile, int col, bool* timed_out) {
           return sum;  // give up; the plan is flagged invalid
         }
         __nanosleep(ns);
-        if (ns < 1024) ns <<= 1;
+        if (ns < 256) ns <<= 1;
         d = ld_desc(&p.desc[static_cast<int64_t>(j - u) * p.ncols + col]);
       }
       sum += static_cast<int>(static_cast<unsigned>(d));
@@ -155,7 +165,7 @@ __device__ bool grid_sync(const PlanDev& p) {
           break;
         }
         __nanosleep(ns);
-        if (ns < 1024) ns <<= 1;
+        if (ns < 128) ns <<= 1;
       }
     }
     __threadfence();
@@ -174,37 +184,50 @@ __device__ __forceinline__ int x_at(const PlanDev& p, int col, int64_t g) {
   return __ldcg(&p.tile_wpre[at]) + __popc(__ldcg(&p.tile_bits[at]) & lanes_below(gl & 31));
 }
 
-// Exclusive scan of n ints in shared memory, one CTA; returns the total.
-__device__ int block_exclusive_scan(int* a, int n, int* scratch /* blockDim.x */) {
-  const int nt = blockDim.x;
-  const int per = (n + nt - 1) / nt;
+// Exclusive scan of n ints in shared memory by one CTA of kTile threads
+// (each thread a contiguous run, warp shuffles across threads); returns the
+// total.  `warp_sums` holds kTile/32 ints.
+__device__ int block_exclusive_scan(int* a, int n, int* warp_sums) {
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int per = (n + kTile - 1) / kTile;
   const int lo = threadIdx.x * per;
   int sum = 0;
   for (int i = 0; i < per; ++i)
     if (lo + i < n) sum += a[lo + i];
-  scratch[threadIdx.x] = sum;
-  __syncthreads();
-  for (int off = 1; off < nt; off <<= 1) {
-    int v = threadIdx.x >= off ? scratch[threadIdx.x - off] : 0;
-    __syncthreads();
-    scratch[threadIdx.x] += v;
-    __syncthreads();
+  int incl = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
   }
-  int run = scratch[threadIdx.x] - sum;
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kTile / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += v;
+    }
+    if (lane < kTile / 32) warp_sums[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  int run = incl - sum + (warp > 0 ? warp_sums[warp - 1] : 0);
   for (int i = 0; i < per; ++i)
     if (lo + i < n) {
-      int v = a[lo + i];
+      const int v = a[lo + i];
       a[lo + i] = run;
       run += v;
     }
-  const int total = scratch[nt - 1];
+  const int total = warp_sums[kTile / 32 - 1];
   __syncthreads();
   return total;
 }
 
 __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   extern __shared__ __align__(16) uint32_t smem[];
-  __shared__ int scan_scratch[kTile];
+  __shared__ int scan_scratch[3][kTile / 32];
 
   // ---------------- phase 1: tiles ----------------
   uint32_t* bits = smem;                                           // [kTileWords * ncols]
@@ -262,9 +285,9 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   }
   for (int d = threadIdx.x; d < p.P; d += blockDim.x) recv_off[d] = __ldcg(&p.totals[d]);
   __syncthreads();
-  const int n_exp = block_exclusive_scan(exp_off, p.E, scan_scratch);
-  const int n_pad = block_exclusive_scan(pad_off, p.E, scan_scratch);
-  const int n_recv = block_exclusive_scan(recv_off, p.P, scan_scratch);
+  const int n_exp = block_exclusive_scan(exp_off, p.E, scan_scratch[0]);
+  const int n_pad = block_exclusive_scan(pad_off, p.E, scan_scratch[1]);
+  const int n_recv = block_exclusive_scan(recv_off, p.P, scan_scratch[2]);
   if (threadIdx.x == 0) {
     exp_off[p.E] = n_exp;
     pad_off[p.E] = n_pad;
@@ -287,38 +310,60 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
 
-  // slot and exp_src
-  for (int64_t i = gtid; i < p.T * p.K; i += nthr) {
-    const int64_t g = i / p.K;
-    const long long v = p.topk_idx[i];
-    int r = -1;
-    if (v >= 0 && v < p.E) {
-      const int e = static_cast<int>(v);
-      r = exp_off[e] + x_at(p, p.P + e, g);
-      p.exp_src[r] = static_cast<int>(g);
+  // slot and exp_src, one token per thread
+  for (int64_t g = gtid; g < p.T; g += nthr) {
+    for (int k = 0; k < p.K; ++k) {
+      const long long v = p.topk_idx[g * p.K + k];
+      int r = -1;
+      if (v >= 0 && v < p.E) {
+        const int e = static_cast<int>(v);
+        r = exp_off[e] + x_at(p, p.P + e, g);
+        p.exp_src[r] = static_cast<int>(g);
+      }
+      p.slot[g * p.K + k] = r;
     }
-    p.slot[i] = r;
   }
 
-  // dense [T,P]: is_token_in_rank, send_head, and recv_src_idx
-  for (int64_t i = gtid; i < p.T * p.P; i += nthr) {
-    const int64_t g = i / p.P;
-    const int d = static_cast<int>(i - g * p.P);
-    const int64_t t = g / kTile;
-    const int gl = static_cast<int>(g - t * kTile);
-    const int64_t at = (t * kTileWords + (gl >> 5)) * p.ncols + d;
-    const uint32_t word = __ldcg(&p.tile_bits[at]);
-    const int bit = (word >> (gl & 31)) & 1;
-    int pos = -1;
-    if (bit) {
-      pos = __ldcg(&p.tile_wpre[at]) + __popc(word & lanes_below(gl & 31));
-      p.recv_src_idx[recv_off[d] + pos] = static_cast<int>(g % p.S);
+  // dense [T,P]: is_token_in_rank, send_head, and recv_src_idx.  One thread
+  // per (32-token word, sub-group of the word, rank d): one bit word and its
+  // prefix, then the sub-group's tokens with a running count.  Threads keep
+  // a fixed d (the stride is a multiple of P), lanes hold consecutive d, so
+  // each store of a token row is coalesced.  The word is split into `sub`
+  // groups so that there are about as many units as threads.
+  {
+    const int64_t words = (p.T + 31) / 32;
+    const int64_t lanes_d = (nthr / p.P) * p.P;  // threads used: a multiple of P
+    int sub = 1;
+    while (sub < 32 && words * sub * p.P < lanes_d) sub <<= 1;
+    const int per = 32 / sub;
+    const int log_sub = __ffs(sub) - 1;
+    if (gtid < lanes_d) {
+      const int d = static_cast<int>(gtid % p.P);
+      const int base = recv_off[d];
+      const int64_t step = lanes_d / p.P;
+      for (int64_t wq = gtid / p.P; wq < words * sub; wq += step) {
+        const int64_t tw = wq >> log_sub;  // word index: tile * kTileWords + warp
+        const int l0 = static_cast<int>(wq & (sub - 1)) * per;
+        const int64_t at = tw * p.ncols + d;
+        const uint32_t word = __ldcg(&p.tile_bits[at]);
+        int pos = __ldcg(&p.tile_wpre[at]) + __popc(word & lanes_below(l0));
+        const int64_t g0 = tw * 32 + l0;
+        const int n_tok = static_cast<int>(min64(per, p.T - g0));
+        int t_local = static_cast<int>(static_cast<uint32_t>(g0) % static_cast<uint32_t>(p.S));
+        for (int l = 0; l < n_tok; ++l) {
+          const int64_t g = g0 + l;
+          const int bit = (word >> (l0 + l)) & 1;
+          p.in_rank[g * p.P + d] = static_cast<unsigned char>(bit);
+          p.send_head[g * p.P + d] = bit ? pos : -1;
+          if (bit) p.recv_src_idx[base + pos++] = t_local;
+          if (++t_local == p.S) t_local = 0;
+        }
+      }
     }
-    p.in_rank[i] = static_cast<unsigned char>(bit);
-    p.send_head[i] = pos;
   }
 
   // prefix matrices, one (s, d, c) per thread; layout of i is [s][d][c]
+#pragma unroll 2
   for (int64_t i = gtid; i < static_cast<int64_t>(p.P) * p.P * p.C; i += nthr) {
     const int c = static_cast<int>(i % p.C);
     const int64_t sd = i / p.C;
@@ -338,10 +383,10 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   }
 
   // per-source expert counts
-  for (int64_t i = gtid; i < static_cast<int64_t>(p.P) * p.E; i += nthr) {
-    const int64_t s = i / p.E;
-    const int e = static_cast<int>(i - s * p.E);
-    p.ntpe[i] = x_at(p, p.P + e, (s + 1) * p.S) - x_at(p, p.P + e, s * p.S);
+  for (int i = static_cast<int>(gtid); i < p.P * p.E; i += static_cast<int>(nthr)) {
+    const int s = i / p.E;
+    const int e = i - s * p.E;
+    p.ntpe[i] = x_at(p, p.P + e, (s + 1) * p.S) - x_at(p, p.P + e, static_cast<int64_t>(s) * p.S);
   }
 
   // padding rows of the expanded layout
@@ -376,7 +421,7 @@ int plan_grid(const PlanDev& p) {
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_plan_kernel, kTile, smem) != cudaSuccess ||
       per_sm < 1)
     return 0;
-  if (per_sm > 4) per_sm = 4;
+  if (per_sm > 2) per_sm = 2;
   cached_grid = per_sm * num_sms();
   cached_smem = smem;
   return cached_grid;
