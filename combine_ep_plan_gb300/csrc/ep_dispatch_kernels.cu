@@ -99,12 +99,42 @@ __device__ __forceinline__ unsigned short cvt_e4m3x2(float lo, float hi) {
   return r;
 }
 
+// x / s rounded to nearest (IEEE binary32), given y = RN(1/s): Markstein's
+// correction (P. Markstein, "Computation of elementary functions on the IBM
+// RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; the division
+// theorem in Muller et al., "Handbook of Floating-Point Arithmetic"): with
+// q0 = RN(x*y) within one ulp of x/s, the remainder r = x - q0*s is exact
+// under FMA and RN(q0 + r*y) = RN(x/s), provided nothing underflows.  The
+// caller guarantees that (see kFastQuotientMinAmax).  A zero x is returned
+// as is, keeping the sign the IEEE quotient has (the remainder step would
+// turn -0 into +0).
+__device__ __forceinline__ float quotient_rn(float x, float s, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r = __fmaf_rn(-q0, s, x);
+  const float q = __fmaf_rn(r, y, q0);
+  return x == 0.0f ? x : q;
+}
+
+// Groups whose amax is at least this use quotient_rn: then scale >= 2^-69 and
+// every remainder of a quotient that can round to a non-zero E4M3 code
+// (|x/s| >= 2^-10) stays a normal number; quotients below 2^-10 round to a
+// signed zero whatever their last bits.  Checked exhaustively, code for
+// code, over every bf16 x and every bf16 amax >= 2^-60 with |x| <= amax.
+// Smaller groups use __fdiv_rn.
+constexpr float kFastQuotientMinAmax = 8.673617379884035e-19f;  // 2^-60
+
 __device__ __forceinline__ float bf16_lo(unsigned w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(unsigned w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Each lane owns 16 consecutive elements (two 16-byte loads, one 16-byte
-// store of codes); eight lanes form one 128-element scale group.  Work item =
-// (row item, chunk of 512 elements), T token rows then N_pad padding rows.
+// FP8 work item = (row item, chunk of kFp8Units*512 elements).  In each unit
+// a lane owns 16 consecutive elements (two 16-byte loads, one 16-byte store
+// of codes) and eight lanes form one 128-element scale group; the chunk's
+// 4*kFp8Units scales are stored by as many lanes in one contiguous store.
+#ifndef EP_FP8_UNITS
+#define EP_FP8_UNITS 4
+#endif
+constexpr int kFp8Units = EP_FP8_UNITS;
+
 __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -112,7 +142,9 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
   const int64_t hv = a.H / 8;     // 16-byte vectors of bf16 per source row
   const int64_t qv = a.H / 16;    // 16-byte vectors of codes per expanded row
   const int64_t groups = a.H / 128;
-  const int64_t chunks = (qv + 31) / 32;
+  constexpr int kUnitVec = 32;                 // 16-element units per warp per unit step
+  constexpr int kChunkVec = kUnitVec * kFp8Units;
+  const int64_t chunks = (qv + kChunkVec - 1) / kChunkVec;
   const int64_t n_pad = a.zero_pad ? a.sizes[kSizePad] : 0;
   const int64_t n_items = (a.T + n_pad) * chunks;
   const uint4* x = static_cast<const uint4*>(a.x);
@@ -120,9 +152,11 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
 
   for (int64_t item = warp; item < n_items; item += nwarps) {
     const int64_t ri = item / chunks;
-    const int64_t qi = (item - ri * chunks) * 32 + lane;  // this lane's 16-element chunk
-    // H % 128 == 0, so an inactive lane takes a whole group of eight lanes with it
-    const bool active = qi < qv;
+    const int64_t q_base = (item - ri * chunks) * kChunkVec;  // first 16-element unit of the chunk
+    const int64_t g_base = q_base / 8;                          // first scale group of the chunk
+    // lanes 0 .. 4*kFp8Units-1 own the chunk's scales, in order
+    const int sc_lane = lane < 4 * kFp8Units ? lane : 0;
+    const bool sc_active = lane < 4 * kFp8Units && g_base + lane < groups;
     if (ri < a.T) {
       const int64_t g = ri;
       int my_row = -1;
@@ -132,41 +166,72 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
         my_row = -1;
       }
       const uint4* src = x + g * hv;
-      uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-      if (active) {
-        lo = ld_stream(src + 2 * qi);
-        hi = ld_stream(src + 2 * qi + 1);
+      uint4 lo[kFp8Units], hi[kFp8Units];
+#pragma unroll
+      for (int u = 0; u < kFp8Units; ++u) {
+        const int64_t qi = q_base + u * kUnitVec + lane;
+        lo[u] = make_uint4(0u, 0u, 0u, 0u);
+        hi[u] = lo[u];
+        if (qi < qv) {
+          lo[u] = ld_stream(src + 2 * qi);
+          hi[u] = ld_stream(src + 2 * qi + 1);
+        }
       }
-      float f[16];
-      const unsigned w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+      uint4 q[kFp8Units];
+      float scale_u[kFp8Units];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        f[2 * i] = bf16_lo(w[i]);
-        f[2 * i + 1] = bf16_hi(w[i]);
+      for (int u = 0; u < kFp8Units; ++u) {
+        float f[16];
+        const unsigned w[8] = {lo[u].x, lo[u].y, lo[u].z, lo[u].w, hi[u].x, hi[u].y, hi[u].z, hi[u].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          f[2 * i] = bf16_lo(w[i]);
+          f[2 * i + 1] = bf16_hi(w[i]);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        const float scale = __fdiv_rn(amax, 448.0f);
+        scale_u[u] = scale;
+        q[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (amax != 0.0f) {
+          unsigned short c[8];
+          if (amax >= kFastQuotientMinAmax && amax <= 3.402823466e38f) {
+            const float y = __frcp_rn(scale);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              c[i] = cvt_e4m3x2(quotient_rn(f[2 * i], scale, y), quotient_rn(f[2 * i + 1], scale, y));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
+          }
+          q[u].x = c[0] | (static_cast<unsigned>(c[1]) << 16);
+          q[u].y = c[2] | (static_cast<unsigned>(c[3]) << 16);
+          q[u].z = c[4] | (static_cast<unsigned>(c[5]) << 16);
+          q[u].w = c[6] | (static_cast<unsigned>(c[7]) << 16);
+        }
       }
-      float amax = 0.0f;
+      // gather the chunk's scales: scale of group j (j = u*4 + m) lives in lane 8*m of unit u
+      float my_scale = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
-      const float scale = __fdiv_rn(amax, 448.0f);
-      uint4 q = make_uint4(0u, 0u, 0u, 0u);
-      if (amax != 0.0f) {
-        unsigned short c[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          c[i] = cvt_e4m3x2(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
-        q.x = c[0] | (static_cast<unsigned>(c[1]) << 16);
-        q.y = c[2] | (static_cast<unsigned>(c[3]) << 16);
-        q.z = c[4] | (static_cast<unsigned>(c[5]) << 16);
-        q.w = c[6] | (static_cast<unsigned>(c[7]) << 16);
+      for (int u = 0; u < kFp8Units; ++u) {
+        const float v = __shfl_sync(0xffffffffu, scale_u[u], (sc_lane & 3) * 8);
+        if ((sc_lane >> 2) == u) my_scale = v;
       }
       for (int k = 0; k < a.K; ++k) {
         const int r = __shfl_sync(0xffffffffu, my_row, k);
-        if (r < 0 || !active) continue;
-        st_row(out + static_cast<int64_t>(r) * qv + qi, q);
-        if ((lane & 7) == 0) a.scales[static_cast<int64_t>(r) * groups + qi / 8] = scale;
+        if (r < 0) continue;
+        uint4* dst = out + static_cast<int64_t>(r) * qv;
+#pragma unroll
+        for (int u = 0; u < kFp8Units; ++u) {
+          const int64_t qi = q_base + u * kUnitVec + lane;
+          if (qi < qv) st_row(dst + qi, q[u]);
+        }
+        if (sc_active) a.scales[static_cast<int64_t>(r) * groups + g_base + lane] = my_scale;
       }
     } else {
       const int r = a.pad_rows[ri - a.T];
@@ -174,10 +239,13 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
         if (lane == 0) atomicOr(a.status, kStCapacity);
         continue;
       }
-      if (active) {
-        st_row(out + static_cast<int64_t>(r) * qv + qi, make_uint4(0u, 0u, 0u, 0u));
-        if ((lane & 7) == 0) a.scales[static_cast<int64_t>(r) * groups + qi / 8] = 0.0f;
+      uint4* dst = out + static_cast<int64_t>(r) * qv;
+#pragma unroll
+      for (int u = 0; u < kFp8Units; ++u) {
+        const int64_t qi = q_base + u * kUnitVec + lane;
+        if (qi < qv) st_row(dst + qi, make_uint4(0u, 0u, 0u, 0u));
       }
+      if (sc_active) a.scales[static_cast<int64_t>(r) * groups + g_base + lane] = 0.0f;
     }
   }
 }
@@ -201,7 +269,7 @@ cudaError_t launch_dispatch_bf16(const DispatchDev& d, cudaStream_t stream) {
 }
 
 cudaError_t launch_dispatch_fp8(const DispatchDev& d, cudaStream_t stream) {
-  const int64_t chunks = (d.H / 16 + 31) / 32;
+  const int64_t chunks = (d.H / 16 + 32 * kFp8Units - 1) / (32 * kFp8Units);
   ep_dispatch_fp8_kernel<<<item_grid(d.T + d.max_pad, chunks), 256, 0, stream>>>(d);
   return cudaGetLastError();
 }

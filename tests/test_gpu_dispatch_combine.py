@@ -290,3 +290,52 @@ def test_round_trip_full_size_sampled(name, kind):
     got = u16(out[torch.from_numpy(toks).cuda()])
     np.testing.assert_allclose(_f32(got), _f32(ref), rtol=RTOL, atol=ATOL)
     assert np.array_equal(got, ref)
+
+
+def _midpoint_stress_rows(T, H, seed):
+    """bf16 rows whose 128-element groups put x/scale within a bf16 ulp of
+    E4M3 rounding midpoints, plus signed zeros, subnormals, and groups below
+    the kernel's fast-quotient threshold (amax < 2^-60)."""
+    rng = np.random.default_rng(seed)
+    codes = np.arange(0, 0x7F, dtype=np.uint8)  # finite non-negative E4M3 codes
+    vals = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy().astype(np.float64)
+    mids = (vals[:-1] + vals[1:]) / 2
+    amaxes = np.array([3.0, 0.7, 1.0e-3, 2.0 ** -60, 2.0 ** -61, 3.0e-25, 1.0e30, 448.0, 5.5, 2.0 ** -126])
+    x = np.zeros((T, H), np.float32)
+    for t in range(T):
+        for j in range(H // 128):
+            amax = amaxes[(t * 7 + j) % len(amaxes)] * (1 + 0.01 * rng.standard_normal())
+            amax = float(torch.tensor(amax, dtype=torch.float32).to(torch.bfloat16).float())
+            s = np.float32(amax) / np.float32(448.0)
+            m = rng.choice(mids, size=127) * rng.choice([-1.0, 1.0], size=127)
+            g = (m * float(s)).astype(np.float32)
+            g = np.clip(g, -amax, amax)
+            g[:3] = [0.0, -0.0, 2.0 ** -130]
+            x[t, j * 128] = amax if t % 2 else -amax
+            x[t, j * 128 + 1:(j + 1) * 128] = g
+    bits = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
+    # nudge by -1/0/+1 bf16 ulp, keeping |x| <= amax of the group
+    nudge = rng.integers(-1, 2, size=bits.shape).astype(np.int32)
+    nudged = (bits.astype(np.int32) + nudge).astype(np.uint16)
+    f0 = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).float().numpy()
+    f1 = torch.from_numpy(nudged.view(np.int16)).view(torch.bfloat16).float().numpy()
+    am = np.abs(f0).reshape(T, H // 128, 128).max(axis=2).repeat(128, axis=1)
+    ok = np.isfinite(f1) & (np.abs(f1) <= am) & (np.sign(f1) == np.sign(f0))
+    ok[:, ::128] = False  # keep the amax element itself
+    bits[ok] = nudged[ok]
+    return bits
+
+
+def test_dispatch_fp8_rounding_midpoints_and_tiny_groups():
+    w = WORKLOADS["tiny"].scaled(H=1280)
+    idx, wts = draw_topk(w)
+    x = _midpoint_stress_rows(w.T, w.H, seed=3)
+    pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
+    q_ref, s_ref = oracle.dispatch_fp8(x, pl)
+    h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
+    recv, scales = ep.dispatch(h, bits_to_bf16_tensor(x).cuda(), "fp8")
+    assert h.sync_status() == ep.EP_OK
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    q = u8(recv)
+    bad = np.argwhere(q != q_ref)
+    assert len(bad) == 0, f"{len(bad)} codes differ, first {bad[:3].tolist()}"
