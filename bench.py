@@ -38,7 +38,6 @@ if ROOT not in sys.path:
 
 METRIC = "dispatch+combine GB/s and tokens/s on 1×GB300; % of HBM roofline"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS_PER_STEP = 3  # plan + dispatch + combine
 
 
 # ---------------------------------------------------------------------------
@@ -104,6 +103,15 @@ def ledger(w, n_exp: int, n_valid: int, n_recv: int, fp8: bool = False) -> dict:
         dispatch = T * H * 2 + n_exp * H * 2 + T * K * 4
     combine = n_valid * H * 2 + T * K * (4 + 4) + T * H * 2
     return {"plan": plan, "dispatch": dispatch, "combine": combine, "total": plan + dispatch + combine}
+
+
+def step_ledger(w, n_exp: int, n_valid: int, n_recv: int) -> dict:
+    """Ledger of one step of a workload: plan, its dispatches, one combine."""
+    led = ledger(w, n_exp, n_valid, n_recv, fp8=w.fp8)
+    n_disp = 1 + w.cached_steps
+    led["dispatches"] = n_disp
+    led["total"] = led["plan"] + n_disp * led["dispatch"] + led["combine"]
+    return led
 
 
 def payload_ledger(w, n_recv: int) -> int:
@@ -221,9 +229,18 @@ def profiled_traffic(kernel: str, kernel_file: str, workload: str):
 # ---------------------------------------------------------------------------
 
 def oracle_pass(w, idx, wts, x):
+    """One step of the workload by the CPU oracle (cached dispatches reuse x)."""
     import oracle
     pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
-    y = oracle.dispatch_bf16(x, pl, True)
+    for _ in range(1 + w.cached_steps):
+        if w.fp8:
+            q, sc = oracle.dispatch_fp8(x, pl, True)
+        else:
+            y = oracle.dispatch_bf16(x, pl, True)
+    if w.expert == "dequant":
+        y = oracle.expert_dequant(q, sc)
+    elif w.expert == "scale":
+        y = oracle.expert_scale(y, pl)
     oracle.combine(y, pl, wts)
     return pl
 
@@ -241,7 +258,7 @@ def oracle_sample(w, min_seconds: float):
         pl = oracle_pass(w, idx, wts, x)
         times.append(time.perf_counter() - t0)
     n_valid = int(np.sum(pl.slot >= 0))
-    led = ledger(w, pl.num_expanded, n_valid, pl.num_recv_total)
+    led = step_ledger(w, pl.num_expanded, n_valid, pl.num_recv_total)
     t = statistics.mean(times)
     return {"gbs": led["total"] / t / 1e9, "tokens_per_s": w.T / t, "seconds_per_pass": t, "passes": len(times)}
 
@@ -255,7 +272,7 @@ def run_reference(args):
     full = WORKLOADS[args.workload]
     # each step is a bounded sample of the workload: fewer tokens per rank, so
     # that warmup + steps take about two minutes of single-threaded CPU time
-    est_full_s = 4.0 * full.T / 16384 * full.H / 7168
+    est_full_s = 4.0 * full.T / 16384 * full.H / 7168 * full.K / 6 * (1 + 0.2 * full.cached_steps)
     budget = 120.0 / max(1, args.steps + args.warmup)
     S = int(max(8, min(full.S, full.S * budget / est_full_s)))
     w = full.scaled(S=S)
@@ -269,7 +286,7 @@ def run_reference(args):
         pl = oracle_pass(w, idx, wts, x)
     dt = time.perf_counter() - t0
     n_valid = int(np.sum(pl.slot >= 0))
-    led = ledger(w, pl.num_expanded, n_valid, pl.num_recv_total)
+    led = step_ledger(w, pl.num_expanded, n_valid, pl.num_recv_total)
     gbs = led["total"] * args.steps / dt / 1e9
     sample = f"{args.workload} workload with S={S} tokens/rank (T={w.T}) per step, single-threaded C oracle"
     line = {
@@ -285,10 +302,19 @@ def run_reference(args):
     return 0
 
 
+def step_description(w) -> str:
+    disp = "FP8 E4M3 dispatch (quantised inside, zero padding)" if w.fp8 else "BF16 dispatch (zero padding)"
+    if w.cached_steps:
+        disp += f" -> {w.cached_steps} cached-handle dispatches with new x"
+    expert = {"identity": "identity expert (the dispatched rows)",
+              "dequant": "expert outputs = dequantised rows (prepared once, outside the timing)",
+              "scale": "expert outputs = rows scaled by 1+e/E (prepared once, outside the timing)"}[w.expert]
+    return f"fresh plan -> {disp} -> {expert} -> combine"
+
+
 def workload_config(w, sample_S=None) -> dict:
     c = {"workload": f"{w.name}: P={w.P} ranks, E={w.E} experts, S={w.S} tokens/rank (T={w.T}), "
-                     f"H={w.H} bf16, top-{w.K} {w.routing}, expert_alignment={w.A}, fresh plan -> dispatch "
-                     f"(zero padding) -> identity expert -> combine",
+                     f"H={w.H} bf16, top-{w.K} {w.routing}, expert_alignment={w.A}; {step_description(w)}",
          "ranks": w.P, "experts": w.E, "tokens": w.T, "hidden": w.H, "topk": w.K, "expert_alignment": w.A,
          "l2": "no flush: inputs larger than L2 (x %.0f MB, expanded rows ~%.2f GB per step)" % (
              w.T * w.H * 2 / 1e6, w.T * w.K * w.H * 2 / 1e9)}
@@ -314,41 +340,56 @@ def run_ours(args):
     ep.load_library()
     w = WORKLOADS[args.workload]
     idx_np, w_np = draw_topk(w)
-    x_np = draw_hidden(w.T, w.H, hidden_seed(w))
+    x_nps = [draw_hidden(w.T, w.H, hidden_seed(w, i)) for i in range(1 + w.cached_steps)]
 
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
     idx_t = torch.from_numpy(idx_np).to(dev)
     wts_t = torch.from_numpy(w_np).to(dev)
-    x_t = bits_to_bf16_tensor(x_np).to(dev)
+    x_ts = [bits_to_bf16_tensor(xn).to(dev) for xn in x_nps]
+    x_t = x_ts[0]
+    out_dtype = "fp8" if w.fp8 else "bf16"
     cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
-    recv = torch.empty((cap, w.H), dtype=torch.bfloat16, device=dev)
+    recv = torch.empty((cap, w.H), dtype=torch.float8_e4m3fn if w.fp8 else torch.bfloat16, device=dev)
+    recv_sc = torch.empty((cap, w.H // 128), dtype=torch.float32, device=dev) if w.fp8 else None
     out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
 
     # one handle, re-planned from topk_idx every step (a fresh plan without
     # allocation: ep_replan recomputes every plan array)
     h = ep.plan(idx_t, w.P, w.E, w.A, stream=stream)
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        h.replan(idx_t, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        ep.dispatch(h, x_t, "bf16", True, recv_x=recv, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
-        ep.combine(h, recv, wts_t, out=out, stream=stream)
-        if ev is not None:
-            ev[3].record(stream)
-        return h
-
-    # sizes for the ledger (outside any timed region)
-    step()
+    ep.dispatch(h, x_t, out_dtype, True, recv_x=recv, recv_scales=recv_sc, stream=stream)
     n_exp, n_recv = h.sizes(stream)
     h.check(stream)
     n_valid = int((idx_t >= 0).sum().item())
-    led = ledger(w, n_exp, n_valid, n_recv)
+    led = step_ledger(w, n_exp, n_valid, n_recv)
+
+    # the expert outputs the combine reads: the dispatched rows themselves
+    # (identity), or rows prepared once here, outside any timed region
+    if w.expert == "identity":
+        y = recv
+    elif w.expert == "dequant":
+        y = (recv.float() * recv_sc.repeat_interleave(128, dim=1)).to(torch.bfloat16)
+    else:
+        e_of_row = torch.repeat_interleave(torch.arange(w.E, device=dev),
+                                           torch.diff(h.field("expert_offsets").long()))
+        y = torch.zeros((cap, w.H), dtype=torch.bfloat16, device=dev)
+        y[: len(e_of_row)] = (recv[: len(e_of_row)].float() * (1.0 + e_of_row.float() / w.E)[:, None]).to(
+            torch.bfloat16)
+
+    def step(ev=None, hh=h, xs=None, idx=idx_t, wts=wts_t, o=out):
+        xs = xs if xs is not None else x_ts
+        if ev is not None:
+            ev[0].record(stream)
+        hh.replan(idx, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        for xi in xs:  # the fresh dispatch, then the cached-handle dispatches with new x
+            ep.dispatch(hh, xi, out_dtype, True, recv_x=recv, recv_scales=recv_sc, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        ep.combine(hh, y, wts, out=o, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -371,25 +412,24 @@ def run_ours(args):
     sampler.mark(t_wall0, t_wall1)
     local_ms = start.elapsed_time(end)
     plan_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
-    disp_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+    disp_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events) / (1 + w.cached_steps)
     comb_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in events)
     agg = aggregate(led["total"], w.T, local_ms, world, args.steps)
 
     # End to end through the public API with host buffers: every step copies
-    # its inputs (x, topk_idx, topk_weights) from pinned host memory to the
-    # device and its combined output back to pinned host memory, inside the
-    # timed region.  Steps are pipelined as a serving loop would run them: the
-    # H2D copy of step i+1 and the D2H copy of step i-1 run on their own
-    # streams (copy engines) while step i computes; device buffers are double
-    # buffered and every reuse waits on the event of the step that used it.
+    # its inputs (x for each dispatch, topk_idx, topk_weights) from pinned host
+    # memory to the device and its combined output back to pinned host memory,
+    # inside the timed region.  Steps are pipelined as a serving loop would run
+    # them: the H2D copies of step i+1 and the D2H copy of step i-1 run on
+    # their own streams (copy engines) while step i computes; device buffers
+    # are double buffered and every reuse waits on the event of the step that
+    # used it.
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    x_pin = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    for b in x_pin:
-        b.copy_(bits_to_bf16_tensor(x_np))
+    x_pin = [[bits_to_bf16_tensor(xn).pin_memory() for xn in x_nps] for _ in range(2)]
     idx_pin = torch.from_numpy(idx_np).pin_memory()
     w_pin = torch.from_numpy(w_np).pin_memory()
     out_pin = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    xs = [x_t, torch.empty_like(x_t)]
+    xss = [x_ts, [torch.empty_like(xt) for xt in x_ts]]
     idxs = [idx_t, torch.empty_like(idx_t)]
     wtss = [wts_t, torch.empty_like(wts_t)]
     outs = [out, torch.empty_like(out)]
@@ -397,7 +437,6 @@ def run_ours(args):
     s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
     def run_e2e(n):
-        ev_in = [None, None]      # inputs of buffer b copied
         ev_done = [None, None]    # compute on buffer b finished
         ev_out = [None, None]     # output of buffer b copied back
         for i in range(n):
@@ -405,17 +444,16 @@ def run_ours(args):
             with torch.cuda.stream(s_h2d):
                 if ev_done[b] is not None:
                     s_h2d.wait_event(ev_done[b])
-                xs[b].copy_(x_pin[b], non_blocking=True)
+                for dst, src in zip(xss[b], x_pin[b]):
+                    dst.copy_(src, non_blocking=True)
                 idxs[b].copy_(idx_pin, non_blocking=True)
                 wtss[b].copy_(w_pin, non_blocking=True)
-                ev_in[b] = torch.cuda.Event()
-                ev_in[b].record(s_h2d)
-            stream.wait_event(ev_in[b])
+                ev_in = torch.cuda.Event()
+                ev_in.record(s_h2d)
+            stream.wait_event(ev_in)
             if ev_out[b] is not None:
                 stream.wait_event(ev_out[b])
-            hs[b].replan(idxs[b], stream=stream)
-            ep.dispatch(hs[b], xs[b], "bf16", True, recv_x=recv, stream=stream)
-            ep.combine(hs[b], recv, wtss[b], out=outs[b], stream=stream)
+            step(hh=hs[b], xs=xss[b], idx=idxs[b], wts=wtss[b], o=outs[b])
             ev_done[b] = torch.cuda.Event()
             ev_done[b].record(stream)
             with torch.cuda.stream(s_d2h):
@@ -447,13 +485,14 @@ def run_ours(args):
         if status != ep.EP_OK:
             raise RuntimeError(f"device status {status} after the timed steps")
         hh.destroy(stream)
-    h2d = x_pin[0].numel() * 2 + idx_pin.numel() * 8 + w_pin.numel() * 4
+    h2d = sum(xp.numel() * 2 for xp in x_pin[0]) + idx_pin.numel() * 8 + w_pin.numel() * 4
     d2h = out_pin[0].numel() * 2
 
     # roofline of the dominant kernel
     peak, peak_src = hbm_peak()
     if disp_ms >= comb_ms:
-        kname, kfile, kbytes, kms = "ep_dispatch_bf16_kernel", "ep_dispatch_kernels.cu", led["dispatch"], disp_ms
+        kname = "ep_dispatch_fp8_kernel" if w.fp8 else "ep_dispatch_bf16_kernel"
+        kfile, kbytes, kms = "ep_dispatch_kernels.cu", led["dispatch"], disp_ms
     else:
         kname, kfile, kbytes, kms = "ep_combine_kernel", "ep_combine_kernels.cu", led["combine"], comb_ms
     achieved = kbytes / (kms / 1e3) / 1e9
@@ -466,8 +505,8 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         s = oracle_sample(w, min_seconds=8.0)
         cpu = {"value": round(s["gbs"], 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"full {w.name} workload (T={w.T}, H={w.H}), {s['passes']} plan+dispatch+combine "
-                         f"pass(es), single-threaded C oracle", "tokens_per_s": round(s["tokens_per_s"], 1)}
+               "sample": f"full {w.name} workload (T={w.T}, H={w.H}), {s['passes']} pass(es) of the step, "
+                         f"single-threaded C oracle", "tokens_per_s": round(s["tokens_per_s"], 1)}
 
     if rank == 0:
         line = {
@@ -488,7 +527,7 @@ def run_ours(args):
                     "api": "C ABI ep_replan/ep_dispatch/ep_combine via the Python binding",
                     "pipeline": "per step: pinned H2D of inputs, plan, dispatch, combine, D2H of the output; "
                                 "copies on their own streams overlap the neighbouring steps' compute"},
-            "gpu_launches": KERNELS_PER_STEP * args.steps,
+            "gpu_launches": (2 + 1 + w.cached_steps) * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
         }

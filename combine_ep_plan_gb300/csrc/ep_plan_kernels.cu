@@ -412,19 +412,27 @@ size_t plan_smem_bytes(int P, int E, int K) {
   return phase1 > phase2 ? phase1 : phase2;
 }
 
+// Co-resident CTAs (at most two per SM, which keeps the grid barrier cheap),
+// and no more than the plan's work needs: one CTA per tile at least, and
+// about one CTA per 1024 phase-2 outputs.
 int plan_grid(const PlanDev& p) {
   const size_t smem = plan_smem_bytes(p.P, p.E, p.K);
   static size_t cached_smem = ~static_cast<size_t>(0);
-  static int cached_grid = 0;
-  if (smem == cached_smem) return cached_grid;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_plan_kernel, kTile, smem) != cudaSuccess ||
-      per_sm < 1)
-    return 0;
-  if (per_sm > 2) per_sm = 2;
-  cached_grid = per_sm * num_sms();
-  cached_smem = smem;
-  return cached_grid;
+  static int cached_cap = 0;
+  if (smem != cached_smem) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_plan_kernel, kTile, smem) != cudaSuccess ||
+        per_sm < 1)
+      return 0;
+    if (per_sm > 2) per_sm = 2;
+    cached_cap = per_sm * num_sms();
+    cached_smem = smem;
+  }
+  const int64_t work = p.T * (p.K + p.P) + static_cast<int64_t>(p.P) * p.P * p.C + static_cast<int64_t>(p.P) * p.E;
+  int64_t grid = (work + 1023) / 1024;
+  if (grid < p.num_tiles) grid = p.num_tiles;
+  if (grid > cached_cap) grid = cached_cap;
+  return static_cast<int>(grid);
 }
 
 cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream) {
