@@ -76,6 +76,10 @@ def _load():
         lib.ep_oracle_expert_scale.restype = None
         lib.ep_oracle_expert_scale_rows.argtypes = [P, i64, P, i64, i32, P]
         lib.ep_oracle_expert_scale_rows.restype = None
+        lib.ep_oracle_dispatch_backward.argtypes = [P, i64, P, i64, i32, P]
+        lib.ep_oracle_dispatch_backward.restype = None
+        lib.ep_oracle_combine_backward.argtypes = [P, P, i64, P, P, i64, P, i64, i32, i32, P, P]
+        lib.ep_oracle_combine_backward.restype = None
         lib.ep_oracle_expert_dequant.argtypes = [P, P, i64, i64, P]
         lib.ep_oracle_expert_dequant.restype = None
         lib.ep_oracle_f32_to_bf16.argtypes = [ctypes.c_float]
@@ -215,6 +219,30 @@ def combine(y_bits: np.ndarray, pl: Plan, topk_weights: np.ndarray) -> np.ndarra
     out = np.zeros((pl.T, H), np.uint16)
     _load().ep_oracle_combine(_ptr(y), H, _ptr(pl.slot), _ptr(w), pl.T, pl.K, _ptr(out))
     return out
+
+
+def dispatch_backward(grad_recv_bits: np.ndarray, pl: Plan) -> np.ndarray:
+    """grad_recv [N_exp,H] bf16 bits -> grad_x [T,H] bf16 bits."""
+    g = np.ascontiguousarray(grad_recv_bits, dtype=np.uint16)
+    H = g.shape[1]
+    out = np.zeros((pl.T, H), np.uint16)
+    _load().ep_oracle_dispatch_backward(_ptr(g), H, _ptr(pl.slot), pl.T, pl.K, _ptr(out))
+    return out
+
+
+def combine_backward(grad_out_bits: np.ndarray, y_bits: np.ndarray, pl: Plan, topk_weights: np.ndarray,
+                     zero_pad: bool = True):
+    """-> (grad_y [N_exp,H] bf16 bits, grad_w [T,K] float64)."""
+    go = np.ascontiguousarray(grad_out_bits, dtype=np.uint16)
+    y = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    H = go.shape[1]
+    n = pl.num_expanded
+    gy = np.zeros((n, H), np.uint16)
+    gw = np.zeros((pl.T, pl.K), np.float64)
+    _load().ep_oracle_combine_backward(_ptr(go), _ptr(y), H, _ptr(pl.slot), _ptr(pl.exp_src), n, _ptr(w),
+                                       pl.T, pl.K, int(zero_pad), _ptr(gy), _ptr(gw))
+    return gy, gw
 
 
 def expert_scale(x_exp_bits: np.ndarray, pl: Plan) -> np.ndarray:

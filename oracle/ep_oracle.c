@@ -464,3 +464,58 @@ void ep_oracle_expert_scale_rows(const uint16_t *x_rows, int64_t H, const int32_
                 : 0;
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Backward on the same handle ([TT] §2.3: the backward of dispatch is a     */
+/* combine, the backward of combine is a dispatch, both on the forward plan) */
+/* ------------------------------------------------------------------------ */
+
+/* Dispatch backward: recv[slot[g,k]] = x[g] for every valid k, so
+ * grad_x[g] = sum over k = 0..K-1 with slot >= 0 of grad_recv[slot[g,k]],
+ * accumulated in fp32 in slot order and rounded once to bf16 (the combine
+ * with unit weights). */
+void ep_oracle_dispatch_backward(const uint16_t *grad_recv, int64_t H, const int32_t *slot,
+                                 int64_t T, int K, uint16_t *grad_x)
+{
+    for (int64_t g = 0; g < T; ++g)
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                int32_t r = slot[g * K + k];
+                if (r >= 0)
+                    acc = acc + ep_oracle_bf16_to_f32(grad_recv[(int64_t)r * H + h]);
+            }
+            grad_x[g * H + h] = ep_oracle_f32_to_bf16(acc);
+        }
+}
+
+/* Combine backward: out[g] = sum_k w[g,k] * y[slot[g,k]], so
+ *   grad_y[slot[g,k]] = bf16_RNE(w[g,k] * float(grad_out[g]))  (fp32 product),
+ *   grad_w[g,k]       = sum_h grad_out[g,h] * y[slot[g,k],h]    (fp64 here),
+ * with grad_w = 0 for an unused slot.  Padding rows of grad_y are zeroed
+ * when zero_pad is set (they receive no gradient), left untouched otherwise. */
+void ep_oracle_combine_backward(const uint16_t *grad_out, const uint16_t *y, int64_t H,
+                                const int32_t *slot, const int32_t *exp_src, int64_t n_rows,
+                                const float *topk_weights, int64_t T, int K, int zero_pad,
+                                uint16_t *grad_y, double *grad_w)
+{
+    if (zero_pad)
+        for (int64_t r = 0; r < n_rows; ++r)
+            if (exp_src[r] < 0)
+                for (int64_t h = 0; h < H; ++h)
+                    grad_y[r * H + h] = 0;
+    for (int64_t g = 0; g < T; ++g)
+        for (int k = 0; k < K; ++k) {
+            int32_t r = slot[g * K + k];
+            double dot = 0.0;
+            if (r >= 0) {
+                float wk = topk_weights[g * K + k];
+                for (int64_t h = 0; h < H; ++h) {
+                    float go = ep_oracle_bf16_to_f32(grad_out[g * H + h]);
+                    grad_y[(int64_t)r * H + h] = ep_oracle_f32_to_bf16(wk * go);
+                    dot += (double)go * (double)ep_oracle_bf16_to_f32(y[(int64_t)r * H + h]);
+                }
+            }
+            grad_w[g * K + k] = dot;
+        }
+}
