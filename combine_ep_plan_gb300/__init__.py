@@ -21,6 +21,7 @@ import torch
 __all__ = [
     "EPError", "EPHandle", "plan", "dispatch", "dispatch_fresh", "dispatch_cached", "combine",
     "worst_expanded_rows", "library_path", "load_library", "FIELDS", "set_lookback_debug",
+    "dispatch_backward", "combine_backward",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -99,6 +100,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
                                       i64, vp, ctypes.POINTER(vp)]
     lib.ep_combine.restype = st
     lib.ep_combine.argtypes = [vp, vp, i64, vp, i64, vp, vp]
+    lib.ep_dispatch_backward.restype = st
+    lib.ep_dispatch_backward.argtypes = [vp, vp, i64, i64, vp, vp]
+    lib.ep_combine_backward.restype = st
+    lib.ep_combine_backward.argtypes = [vp, vp, vp, i64, vp, i64, i32, vp, i64, vp, vp]
     lib.ep_sync_status.restype = st
     lib.ep_sync_status.argtypes = [vp, vp]
     lib.ep_handle_get.restype = st
@@ -340,6 +345,46 @@ def combine(handle: EPHandle, y: torch.Tensor, topk_weights: torch.Tensor,
     _check(_lib().ep_combine(handle.ptr, y.data_ptr(), y.shape[0], topk_weights.data_ptr(), H,
                              out.data_ptr(), _stream_ptr(stream)), "ep_combine")
     return out
+
+
+def dispatch_backward(handle: EPHandle, grad_recv: torch.Tensor, grad_x: Optional[torch.Tensor] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Backward of dispatch on the same handle: grad_recv [rows,H] -> grad_x [T,H]."""
+    _need(grad_recv, "grad_recv", torch.bfloat16, 2)
+    H = grad_recv.shape[1]
+    if grad_x is None:
+        grad_x = torch.empty((handle.T, H), dtype=torch.bfloat16, device=grad_recv.device)
+    _need(grad_x, "grad_x", torch.bfloat16, 2)
+    if tuple(grad_x.shape) != (handle.T, H):
+        raise ValueError("grad_x must be [T,H]")
+    _check(_lib().ep_dispatch_backward(handle.ptr, grad_recv.data_ptr(), grad_recv.shape[0], H, grad_x.data_ptr(),
+                                       _stream_ptr(stream)), "ep_dispatch_backward")
+    return grad_x
+
+
+def combine_backward(handle: EPHandle, grad_out: torch.Tensor, y: torch.Tensor, topk_weights: torch.Tensor,
+                     zero_pad: bool = True, grad_y: Optional[torch.Tensor] = None,
+                     grad_weights: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None):
+    """Backward of combine on the same handle -> (grad_y [rows,H] bf16, grad_weights [T,K] f32)."""
+    _need(grad_out, "grad_out", torch.bfloat16, 2)
+    _need(y, "y", torch.bfloat16, 2)
+    _need(topk_weights, "topk_weights", torch.float32, 2)
+    H = grad_out.shape[1]
+    if tuple(grad_out.shape) != (handle.T, H) or y.shape[1] != H:
+        raise ValueError("grad_out must be [T,H] and y [rows,H]")
+    if tuple(topk_weights.shape) != (handle.T, handle.K):
+        raise ValueError("topk_weights must be [T,K]")
+    if grad_y is None:
+        grad_y = torch.empty_like(y)
+    if grad_weights is None:
+        grad_weights = torch.empty((handle.T, handle.K), dtype=torch.float32, device=y.device)
+    _need(grad_y, "grad_y", torch.bfloat16, 2)
+    _need(grad_weights, "grad_weights", torch.float32, 2)
+    _check(_lib().ep_combine_backward(handle.ptr, grad_out.data_ptr(), y.data_ptr(), y.shape[0],
+                                      topk_weights.data_ptr(), H, int(bool(zero_pad)), grad_y.data_ptr(),
+                                      grad_y.shape[0], grad_weights.data_ptr(), _stream_ptr(stream)),
+           "ep_combine_backward")
+    return grad_y, grad_weights
 
 
 def set_lookback_debug(poll_limit: int = 0, suppress_tile: int = -1):

@@ -366,6 +366,51 @@ ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, const float
   return cuda_status(ep::launch_combine(c, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+ep_status_t ep_dispatch_backward(ep_handle_t h, const void* grad_recv, int64_t grad_rows, int64_t H,
+                                 void* grad_x, ep_stream_t stream) {
+  if (!h || !grad_recv || !grad_x || grad_rows < 0 || H < 8 || H % 8 != 0) return EP_ERR_INVALID;
+  if (!aligned(grad_recv, 16) || !aligned(grad_x, 16)) return EP_ERR_INVALID;
+  ep::CombineDev c;
+  c.y = grad_recv;
+  c.slot = h->dev.slot;
+  c.weights = nullptr;  // unit weights: the sum over the token's expanded rows
+  c.status = h->dev.ctr + ep::kCtrStatus;
+  c.out = grad_x;
+  c.T = h->dev.T;
+  c.K = h->dev.K;
+  c.H = H;
+  c.y_rows = grad_rows;
+  return cuda_status(ep::launch_combine(c, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ep_status_t ep_combine_backward(ep_handle_t h, const void* grad_out, const void* y, int64_t y_rows,
+                                const float* w, int64_t H, int zero_pad, void* grad_y, int64_t grad_y_rows,
+                                float* grad_w, ep_stream_t stream) {
+  if (!h || !grad_out || !y || !w || !grad_y || !grad_w || y_rows < 0 || grad_y_rows < 0 || H < 8 ||
+      H % 8 != 0)
+    return EP_ERR_INVALID;
+  if (!aligned(grad_out, 16) || !aligned(y, 16) || !aligned(grad_y, 16) || !aligned(w, 4) ||
+      !aligned(grad_w, 4))
+    return EP_ERR_INVALID;
+  ep::CombineBwdDev c;
+  c.grad_out = grad_out;
+  c.y = y;
+  c.slot = h->dev.slot;
+  c.weights = w;
+  c.pad_rows = h->dev.pad_rows;
+  c.sizes = h->dev.sizes;
+  c.status = h->dev.ctr + ep::kCtrStatus;
+  c.grad_y = grad_y;
+  c.grad_w = grad_w;
+  c.T = h->dev.T;
+  c.K = h->dev.K;
+  c.H = H;
+  c.y_rows = y_rows;
+  c.grad_y_rows = grad_y_rows;
+  c.max_pad = zero_pad ? h->cap_pad : 0;
+  return cuda_status(ep::launch_combine_backward(c, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 ep_status_t ep_sync_status(ep_handle_t h, ep_stream_t stream) {
   if (!h) return EP_ERR_INVALID;
   return read_status_word(h, reinterpret_cast<cudaStream_t>(stream), true, nullptr);

@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(256, MINB) ep_combine_kernel(CombineDev c) {
     float my_w = 0.0f;
     if (lane < c.K) {
       my_row = c.slot[g * c.K + lane];
-      my_w = c.weights[g * c.K + lane];
+      my_w = c.weights ? c.weights[g * c.K + lane] : 1.0f;
       if (my_row >= c.y_rows) {
         atomicOr(c.status, kStCapacity);
         my_row = -1;
@@ -122,7 +122,125 @@ cudaError_t launch_k(const CombineDev& c, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// Combine backward, one CTA of 128 threads per token: grad_out[g] is read
+// once; for each slot k the row y[slot] is read for the dot product grad_w =
+// <grad_out[g], y[slot]> and grad_y[slot] = bf16(w * grad_out[g]) is written.
+// The dot products are summed per thread over its vectors, then by a fixed
+// shuffle tree per warp and over the four warps in order: deterministic.
+// CTAs beyond T zero the padding rows of grad_y.
+template <int KMAX>
+__global__ void __launch_bounds__(128) ep_combine_backward_kernel(CombineBwdDev c) {
+  constexpr int kWarps = 4;
+  __shared__ int s_row[KMAX];
+  __shared__ float s_w[KMAX];
+  __shared__ float s_dot[kWarps][KMAX];
+  const int64_t hv = c.H / 8;
+  uint4* gy = static_cast<uint4*>(c.grad_y);
+  const int64_t item = blockIdx.x;
+  if (item >= c.T) {
+    const int64_t pi = item - c.T;
+    if (pi >= c.sizes[kSizePad]) return;
+    const int r = c.pad_rows[pi];
+    if (r >= c.grad_y_rows) {
+      if (threadIdx.x == 0) atomicOr(c.status, kStCapacity);
+      return;
+    }
+    for (int64_t v = threadIdx.x; v < hv; v += blockDim.x)
+      gy[static_cast<int64_t>(r) * hv + v] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const int64_t g = item;
+  if (threadIdx.x < KMAX) {
+    const int k = threadIdx.x;
+    int r = -1;
+    float wk = 0.0f;
+    if (k < c.K) {
+      r = c.slot[g * c.K + k];
+      wk = c.weights[g * c.K + k];
+      if (r >= c.y_rows || r >= c.grad_y_rows) {
+        atomicOr(c.status, kStCapacity);
+        r = -1;
+      }
+    }
+    s_row[k] = r;
+    s_w[k] = wk;
+  }
+  __syncthreads();
+  int row[KMAX];
+  float wk[KMAX], dot[KMAX];
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    row[k] = s_row[k];
+    wk[k] = s_w[k];
+    dot[k] = 0.0f;
+  }
+  const uint4* go_row = static_cast<const uint4*>(c.grad_out) + g * hv;
+  const uint4* y = static_cast<const uint4*>(c.y);
+  for (int64_t v = threadIdx.x; v < hv; v += blockDim.x) {
+    const uint4 go = ld_stream(go_row + v);
+    uint4 yv[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (row[k] >= 0) yv[k] = ld_stream(y + static_cast<int64_t>(row[k]) * hv + v);
+    const unsigned gw[4] = {go.x, go.y, go.z, go.w};
+    float gof[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      gof[2 * i] = __uint_as_float(gw[i] << 16);
+      gof[2 * i + 1] = __uint_as_float(gw[i] & 0xffff0000u);
+    }
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      if (row[k] < 0) continue;
+      const unsigned yw[4] = {yv[k].x, yv[k].y, yv[k].z, yv[k].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        dot[k] = fmaf(gof[2 * i], __uint_as_float(yw[i] << 16), dot[k]);
+        dot[k] = fmaf(gof[2 * i + 1], __uint_as_float(yw[i] & 0xffff0000u), dot[k]);
+      }
+      uint4 o;
+      o.x = pack_bf16x2(__fmul_rn(wk[k], gof[0]), __fmul_rn(wk[k], gof[1]));
+      o.y = pack_bf16x2(__fmul_rn(wk[k], gof[2]), __fmul_rn(wk[k], gof[3]));
+      o.z = pack_bf16x2(__fmul_rn(wk[k], gof[4]), __fmul_rn(wk[k], gof[5]));
+      o.w = pack_bf16x2(__fmul_rn(wk[k], gof[6]), __fmul_rn(wk[k], gof[7]));
+      gy[static_cast<int64_t>(row[k]) * hv + v] = o;
+    }
+  }
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    float d = dot[k];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    if (lane == 0) s_dot[warp][k] = d;
+  }
+  __syncthreads();
+  if (threadIdx.x < c.K) {
+    const int k = threadIdx.x;
+    float d = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) d += s_dot[w][k];
+    c.grad_w[g * c.K + k] = row[k] >= 0 ? d : 0.0f;
+  }
+}
+
+template <int KMAX>
+cudaError_t launch_bwd(const CombineBwdDev& c, cudaStream_t stream) {
+  const int64_t blocks = c.T + c.max_pad;
+  ep_combine_backward_kernel<KMAX><<<static_cast<unsigned>(blocks), 128, 0, stream>>>(c);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_combine_backward(const CombineBwdDev& c, cudaStream_t stream) {
+  if (c.K <= 2) return launch_bwd<2>(c, stream);
+  if (c.K <= 4) return launch_bwd<4>(c, stream);
+  if (c.K <= 6) return launch_bwd<6>(c, stream);
+  if (c.K <= 8) return launch_bwd<8>(c, stream);
+  return launch_bwd<16>(c, stream);
+}
 
 cudaError_t launch_combine(const CombineDev& c, cudaStream_t stream) {
   switch (c.K) {

@@ -97,7 +97,7 @@ cudaError_t launch_dispatch_fp8(const DispatchDev& d, cudaStream_t stream);
 struct CombineDev {
   const void* y;          // [y_rows,H] bf16
   const int* slot;        // [T,K]
-  const float* weights;   // [T,K]
+  const float* weights;   // [T,K]; NULL: unit weights (the dispatch backward)
   unsigned* status;
   void* out;              // [T,H] bf16
   int64_t T;
@@ -106,6 +106,25 @@ struct CombineDev {
   int64_t y_rows;
 };
 cudaError_t launch_combine(const CombineDev& c, cudaStream_t stream);
+
+struct CombineBwdDev {
+  const void* grad_out;   // [T,H] bf16
+  const void* y;          // [y_rows,H] bf16
+  const int* slot;        // [T,K]
+  const float* weights;   // [T,K]
+  const int* pad_rows;    // [N_pad]
+  const int* sizes;       // device sizes (N_pad)
+  unsigned* status;
+  void* grad_y;           // [grad_y_rows,H] bf16
+  float* grad_w;          // [T,K]
+  int64_t T;
+  int K;
+  int64_t H;
+  int64_t y_rows;
+  int64_t grad_y_rows;
+  int64_t max_pad;        // upper bound of N_pad, 0 without zero padding
+};
+cudaError_t launch_combine_backward(const CombineBwdDev& c, cudaStream_t stream);
 
 int num_sms();
 

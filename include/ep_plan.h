@@ -214,6 +214,40 @@ ep_status_t ep_combine(ep_handle_t handle, const void *y_dev, int64_t y_rows,
                        ep_stream_t stream);
 
 /*
+ * ep_dispatch_backward — the backward of dispatch, which is a combine on the
+ * same handle ([TT] §2.3): every forward row recv[slot[g,k]] is a copy of
+ * x[g], so grad_x[g] = bf16_RNE( sum over k = 0..K-1 with slot[g,k] >= 0, in
+ * that order, of float(grad_recv[slot[g,k]]) ), accumulated in fp32.
+ *
+ * grad_recv_dev  [grad_rows,H] bfloat16 gradient of the expanded rows, 16-byte
+ *                aligned, H % 8 == 0; padding rows are never read; a slot at or
+ *                beyond grad_rows records EP_ERR_CAPACITY and is skipped.
+ * grad_x_dev     [T,H] bfloat16 output, 16-byte aligned.
+ */
+ep_status_t ep_dispatch_backward(ep_handle_t handle, const void *grad_recv_dev, int64_t grad_rows,
+                                 int64_t hidden, void *grad_x_dev, ep_stream_t stream);
+
+/*
+ * ep_combine_backward — the backward of combine, which is a dispatch on the
+ * same handle ([TT] §2.3).  With out[g] = sum_k w[g,k] * y[slot[g,k]]:
+ *   grad_y[slot[g,k]] = bf16_RNE(w[g,k] * float(grad_out[g]))  (fp32 product),
+ *   grad_w[g,k]       = <grad_out[g], y[slot[g,k]]>, fp32, summed in a fixed
+ *                       order (deterministic; 0 for an unused slot).
+ * grad_out_dev   [T,H] bfloat16, 16-byte aligned, H % 8 == 0.
+ * y_dev          [y_rows,H] bfloat16 forward expert outputs, 16-byte aligned.
+ * topk_weights_dev [T,K] float32.
+ * zero_pad       nonzero: padding rows of grad_y are zeroed; 0: untouched.
+ * grad_y_dev     [grad_y_rows,H] bfloat16 output, 16-byte aligned.
+ * grad_weights_dev [T,K] float32 output.
+ * A slot at or beyond y_rows or grad_y_rows records EP_ERR_CAPACITY and is
+ * skipped.
+ */
+ep_status_t ep_combine_backward(ep_handle_t handle, const void *grad_out_dev, const void *y_dev,
+                                int64_t y_rows, const float *topk_weights_dev, int64_t hidden,
+                                int zero_pad, void *grad_y_dev, int64_t grad_y_rows,
+                                float *grad_weights_dev, ep_stream_t stream);
+
+/*
  * ep_sync_status — synchronises `stream`, returns the first error recorded in
  * the handle's device status word (EP_OK if none) and clears it.
  */
