@@ -76,6 +76,12 @@ def _load():
         lib.ep_oracle_expert_scale.restype = None
         lib.ep_oracle_expert_scale_rows.argtypes = [P, i64, P, i64, i32, P]
         lib.ep_oracle_expert_scale_rows.restype = None
+        lib.ep_oracle_combine_bias.argtypes = [P, i64, P, P, P, i64, i32, P]
+        lib.ep_oracle_combine_bias.restype = None
+        lib.ep_oracle_dispatch_metadata.argtypes = [P, P, i64, i32, i64, P, P]
+        lib.ep_oracle_dispatch_metadata.restype = None
+        lib.ep_oracle_dispatch_fp8_input.argtypes = [P, P, i64, P, i64, i32, P, P]
+        lib.ep_oracle_dispatch_fp8_input.restype = None
         lib.ep_oracle_dispatch_backward.argtypes = [P, i64, P, i64, i32, P]
         lib.ep_oracle_dispatch_backward.restype = None
         lib.ep_oracle_combine_backward.argtypes = [P, P, i64, P, P, i64, P, i64, i32, i32, P, P]
@@ -211,14 +217,41 @@ def dispatch_fp8(x_bits: np.ndarray, pl: Plan, zero_pad: bool = True):
     return q, sc
 
 
-def combine(y_bits: np.ndarray, pl: Plan, topk_weights: np.ndarray) -> np.ndarray:
-    """y_bits: [N_exp,H] uint16 bf16; topk_weights [T,K] f32 -> [T,H] uint16 bf16."""
+def combine(y_bits: np.ndarray, pl: Plan, topk_weights: np.ndarray, bias_bits: np.ndarray = None) -> np.ndarray:
+    """y_bits: [N_exp,H] uint16 bf16; topk_weights [T,K] f32; optional bias
+    [T,H] bf16 bits -> [T,H] uint16 bf16."""
     y = np.ascontiguousarray(y_bits, dtype=np.uint16)
     w = np.ascontiguousarray(topk_weights, dtype=np.float32)
     H = y.shape[1]
     out = np.zeros((pl.T, H), np.uint16)
-    _load().ep_oracle_combine(_ptr(y), H, _ptr(pl.slot), _ptr(w), pl.T, pl.K, _ptr(out))
+    if bias_bits is None:
+        _load().ep_oracle_combine(_ptr(y), H, _ptr(pl.slot), _ptr(w), pl.T, pl.K, _ptr(out))
+    else:
+        b = np.ascontiguousarray(bias_bits, dtype=np.uint16)
+        _load().ep_oracle_combine_bias(_ptr(y), H, _ptr(pl.slot), _ptr(w), _ptr(b), pl.T, pl.K, _ptr(out))
     return out
+
+
+def dispatch_metadata(pl: Plan, topk_weights: np.ndarray):
+    """-> (recv_weights [N_exp] f32, recv_meta [N_exp,2] i32 = {source token, slot k})."""
+    w = np.ascontiguousarray(topk_weights, dtype=np.float32)
+    n = pl.num_expanded
+    rw = np.zeros(n, np.float32)
+    rm = np.zeros((n, 2), np.int32)
+    _load().ep_oracle_dispatch_metadata(_ptr(pl.slot), _ptr(w), pl.T, pl.K, n, _ptr(rw), _ptr(rm))
+    return rw, rm
+
+
+def dispatch_fp8_input(xq: np.ndarray, xs: np.ndarray, pl: Plan, zero_pad: bool = True):
+    """Pre-quantised input: codes [T,H] u8 + scales [T,H/128] f32 -> expanded rows."""
+    q = np.ascontiguousarray(xq, dtype=np.uint8)
+    s = np.ascontiguousarray(xs, dtype=np.float32)
+    H = q.shape[1]
+    n = pl.num_expanded
+    oq = np.zeros((n, H), np.uint8)
+    osc = np.zeros((n, H // 128), np.float32)
+    _load().ep_oracle_dispatch_fp8_input(_ptr(q), _ptr(s), H, _ptr(pl.exp_src), n, int(zero_pad), _ptr(oq), _ptr(osc))
+    return oq, osc
 
 
 def dispatch_backward(grad_recv_bits: np.ndarray, pl: Plan) -> np.ndarray:

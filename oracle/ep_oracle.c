@@ -403,8 +403,28 @@ void ep_oracle_dispatch_fp8(const uint16_t *x, int64_t H, const int32_t *exp_src
 
 /* Weighted k-way reduction back to token order ([TT] §4.5): widen each bf16
  * expert output to fp32, accumulate in fixed slot order k = 0..K-1 with a
- * fused multiply-add, round once to bf16.  A token without a valid slot
- * gives zeros. */
+ * fused multiply-add, then add the optional bias row ([TT] §3.3, the fused
+ * residual / shared-expert output) in fp32, round once to bf16.  A token
+ * without a valid slot gives its bias (zeros without bias). */
+void ep_oracle_combine_bias(const uint16_t *y, int64_t H, const int32_t *slot,
+                            const float *topk_weights, const uint16_t *bias, int64_t T, int K,
+                            uint16_t *out)
+{
+    for (int64_t g = 0; g < T; ++g)
+        for (int64_t h = 0; h < H; ++h) {
+            float acc = 0.0f;
+            for (int k = 0; k < K; ++k) {
+                int32_t r = slot[g * K + k];
+                if (r < 0)
+                    continue;
+                acc = fmaf(topk_weights[g * K + k], ep_oracle_bf16_to_f32(y[(int64_t)r * H + h]), acc);
+            }
+            if (bias)
+                acc = acc + ep_oracle_bf16_to_f32(bias[g * H + h]);
+            out[g * H + h] = ep_oracle_f32_to_bf16(acc);
+        }
+}
+
 void ep_oracle_combine(const uint16_t *y, int64_t H, const int32_t *slot,
                        const float *topk_weights, int64_t T, int K, uint16_t *out)
 {
@@ -518,4 +538,49 @@ void ep_oracle_combine_backward(const uint16_t *grad_out, const uint16_t *y, int
             }
             grad_w[g * K + k] = dot;
         }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Metadata-carrying dispatch and pre-quantised FP8 input                    */
+/* ------------------------------------------------------------------------ */
+
+/* Per expanded row, the metadata the pages carry next to the hidden bytes
+ * ([TT] §2.1, §4.2: routing weight and source token): recv_weights[r] =
+ * w[g,k] and recv_meta[r] = {g, k} for r = slot[g,k]; padding rows get
+ * weight 0 and {-1, -1}. */
+void ep_oracle_dispatch_metadata(const int32_t *slot, const float *topk_weights, int64_t T, int K,
+                                 int64_t n_rows, float *recv_weights, int32_t *recv_meta)
+{
+    for (int64_t r = 0; r < n_rows; ++r) {
+        recv_weights[r] = 0.0f;
+        recv_meta[2 * r] = -1;
+        recv_meta[2 * r + 1] = -1;
+    }
+    for (int64_t g = 0; g < T; ++g)
+        for (int k = 0; k < K; ++k) {
+            int32_t r = slot[g * K + k];
+            if (r < 0)
+                continue;
+            recv_weights[r] = topk_weights[g * K + k];
+            recv_meta[2 * r] = (int32_t)g;
+            recv_meta[2 * r + 1] = k;
+        }
+}
+
+/* Dispatch of input that is already FP8 ([TT] §3.6: x arrives as (codes,
+ * scales)): expanded row r holds the codes and the H/128 fp32 scales of
+ * token exp_src[r]; padding rows are zero when zero_pad is set. */
+void ep_oracle_dispatch_fp8_input(const uint8_t *xq, const float *xs, int64_t H, const int32_t *exp_src,
+                                  int64_t n_rows, int zero_pad, uint8_t *out_q, float *out_scales)
+{
+    const int64_t G = H / 128;
+    for (int64_t r = 0; r < n_rows; ++r) {
+        int32_t g = exp_src[r];
+        if (g < 0 && !zero_pad)
+            continue;
+        for (int64_t h = 0; h < H; ++h)
+            out_q[r * H + h] = g >= 0 ? xq[(int64_t)g * H + h] : 0;
+        for (int64_t j = 0; j < G; ++j)
+            out_scales[r * G + j] = g >= 0 ? xs[(int64_t)g * G + j] : 0.0f;
+    }
 }
