@@ -491,7 +491,7 @@ def run_ours(args):
     # roofline of the dominant kernel
     peak, peak_src = hbm_peak()
     if disp_ms >= comb_ms:
-        kname = "ep_dispatch_fp8_kernel" if w.fp8 else "ep_dispatch_bf16_kernel"
+        kname = "ep_dispatch_fp8_kernel" if w.fp8 else "ep_dispatch_copy_kernel"
         kfile, kbytes, kms = "ep_dispatch_kernels.cu", led["dispatch"], disp_ms
     else:
         kname, kfile, kbytes, kms = "ep_combine_kernel", "ep_combine_kernels.cu", led["combine"], comb_ms

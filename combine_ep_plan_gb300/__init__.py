@@ -21,7 +21,7 @@ import torch
 __all__ = [
     "EPError", "EPHandle", "plan", "dispatch", "dispatch_fresh", "dispatch_cached", "combine",
     "worst_expanded_rows", "library_path", "load_library", "FIELDS", "set_lookback_debug",
-    "dispatch_backward", "combine_backward",
+    "dispatch_backward", "combine_backward", "dispatch_metadata",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -29,6 +29,7 @@ _LIB_PATH = os.path.join(_PKG, "libep_gb300.so")
 
 EP_OK, EP_ERR_INVALID, EP_ERR_CAPACITY, EP_ERR_TIMEOUT, EP_ERR_CUDA, EP_ERR_MISMATCH, EP_ERR_OOM = range(7)
 EP_DTYPE_BF16, EP_DTYPE_FP8_E4M3 = 0, 1
+EP_DISPATCH_ZERO_PAD, EP_DISPATCH_SCALES_COL_MAJOR = 1, 2
 
 # field name -> (enum value, torch dtype)
 FIELDS = {
@@ -92,14 +93,16 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ep_worst_expanded_rows.restype = i64
     lib.ep_worst_expanded_rows.argtypes = [i64, i32, i32, i32]
     lib.ep_dispatch.restype = st
-    lib.ep_dispatch.argtypes = [vp, vp, i64, i32, i32, vp, vp, i64, vp]
+    lib.ep_dispatch.argtypes = [vp, vp, i32, vp, i64, i32, i32, vp, vp, i64, vp]
     lib.ep_dispatch_cached.restype = st
-    lib.ep_dispatch_cached.argtypes = [vp, i32, i32, i64, vp, i64, i32, i32, vp, vp, i64, vp]
+    lib.ep_dispatch_cached.argtypes = [vp, i32, i32, i64, vp, i32, vp, i64, i32, i32, vp, vp, i64, vp]
     lib.ep_dispatch_fresh.restype = st
-    lib.ep_dispatch_fresh.argtypes = [vp, i64, i32, i32, i32, i32, i32, vp, i64, i32, i32, vp, vp,
+    lib.ep_dispatch_fresh.argtypes = [vp, i64, i32, i32, i32, i32, i32, vp, i32, vp, i64, i32, i32, vp, vp,
                                       i64, vp, ctypes.POINTER(vp)]
+    lib.ep_dispatch_metadata.restype = st
+    lib.ep_dispatch_metadata.argtypes = [vp, vp, vp, vp, i64, i32, vp]
     lib.ep_combine.restype = st
-    lib.ep_combine.argtypes = [vp, vp, i64, vp, i64, vp, vp]
+    lib.ep_combine.argtypes = [vp, vp, i64, vp, vp, i64, vp, vp]
     lib.ep_dispatch_backward.restype = st
     lib.ep_dispatch_backward.argtypes = [vp, vp, i64, i64, vp, vp]
     lib.ep_combine_backward.restype = st
@@ -238,12 +241,16 @@ def worst_expanded_rows(num_tokens: int, num_topk: int, num_experts: int, expert
     return int(_lib().ep_worst_expanded_rows(num_tokens, num_topk, num_experts, expert_alignment))
 
 
-def _dispatch_outputs(H, out_dtype, recv_x, recv_scales, capacity, device):
+def _dispatch_outputs(H, out_dtype, recv_x, recv_scales, capacity, device, col_major):
     if recv_x is None:
         dt = torch.bfloat16 if out_dtype == "bf16" else torch.float8_e4m3fn
         recv_x = torch.empty((capacity, H), dtype=dt, device=device)
     if out_dtype == "fp8" and recv_scales is None:
-        recv_scales = torch.empty((recv_x.shape[0], H // 128), dtype=torch.float32, device=device)
+        rows = recv_x.shape[0]
+        if col_major:  # [rows, H/128] view of a [H/128, rows] buffer: strides (1, rows)
+            recv_scales = torch.empty((H // 128, rows), dtype=torch.float32, device=device).t()
+        else:
+            recv_scales = torch.empty((rows, H // 128), dtype=torch.float32, device=device)
     return recv_x, recv_scales
 
 
@@ -255,34 +262,67 @@ def _dtype_code(out_dtype: str) -> int:
     raise ValueError("out_dtype must be 'bf16' or 'fp8'")
 
 
-def _check_dispatch(x, recv_x, recv_scales, out_dtype):
-    _need(x, "x", torch.bfloat16, 2)
+def _input_code(x: torch.Tensor, x_scales: Optional[torch.Tensor]):
+    if x.dtype == torch.bfloat16:
+        if x_scales is not None:
+            raise ValueError("x_scales only goes with pre-quantised float8_e4m3fn input")
+        return EP_DTYPE_BF16
+    if x.dtype == torch.float8_e4m3fn:
+        if x_scales is None:
+            raise ValueError("pre-quantised input needs x_scales [T, H/128] float32")
+        _need(x_scales, "x_scales", torch.float32, 2)
+        if tuple(x_scales.shape) != (x.shape[0], x.shape[1] // 128):
+            raise ValueError("x_scales must be [T, H/128]")
+        return EP_DTYPE_FP8_E4M3
+    raise TypeError("x must be bfloat16 or float8_e4m3fn")
+
+
+def _check_dispatch(x, recv_x, recv_scales, out_dtype, col_major):
+    if not isinstance(x, torch.Tensor) or not x.is_cuda or x.dim() != 2 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous 2-d CUDA tensor")
     want = torch.bfloat16 if out_dtype == "bf16" else torch.float8_e4m3fn
     _need(recv_x, "recv_x", want, 2)
     if recv_x.shape[1] != x.shape[1]:
         raise ValueError("recv_x hidden size differs from x")
     if out_dtype == "fp8":
-        _need(recv_scales, "recv_scales", torch.float32, 2)
-        if recv_scales.shape[0] < recv_x.shape[0] or recv_scales.shape[1] != x.shape[1] // 128:
+        if recv_scales is None or recv_scales.dtype != torch.float32 or not recv_scales.is_cuda:
+            raise TypeError("recv_scales must be a float32 CUDA tensor")
+        if tuple(recv_scales.shape) != (recv_x.shape[0], x.shape[1] // 128):
             raise ValueError("recv_scales must be [rows, H/128]")
+        if col_major and not recv_scales.t().is_contiguous():
+            raise ValueError("column-major recv_scales must have strides (1, rows)")
+        if not col_major and not recv_scales.is_contiguous():
+            raise ValueError("row-major recv_scales must be contiguous")
+    elif col_major:
+        raise ValueError("column-major scales need FP8 output")
+
+
+def _flags(zero_pad: bool, col_major: bool) -> int:
+    return (EP_DISPATCH_ZERO_PAD if zero_pad else 0) | (EP_DISPATCH_SCALES_COL_MAJOR if col_major else 0)
 
 
 def dispatch(handle: EPHandle, x: torch.Tensor, out_dtype: str = "bf16", zero_pad: bool = True,
              recv_x: Optional[torch.Tensor] = None, recv_scales: Optional[torch.Tensor] = None,
-             capacity: Optional[int] = None, stream: Optional[torch.cuda.Stream] = None):
-    """Row scatter of x [T,H] bf16 into the expanded layout.
+             capacity: Optional[int] = None, stream: Optional[torch.cuda.Stream] = None,
+             x_scales: Optional[torch.Tensor] = None, scales_col_major: bool = False):
+    """Row scatter of x [T,H] (bf16, or float8_e4m3fn with x_scales) into the
+    expanded layout.
 
     Without recv_x, the output is allocated with the exact row count, which
     synchronises the stream once (ep_plan_sizes); pass recv_x (e.g. sized by
     worst_expanded_rows) to avoid that.  Returns (recv_x, recv_scales|None).
     """
     code = _dtype_code(out_dtype)
+    xcode = _input_code(x, x_scales)
     H = x.shape[1]
     if recv_x is None and capacity is None:
         capacity = handle.sizes(stream)[0]
-    recv_x, recv_scales = _dispatch_outputs(H, out_dtype, recv_x, recv_scales, capacity, x.device)
-    _check_dispatch(x, recv_x, recv_scales, out_dtype)
-    _check(_lib().ep_dispatch(handle.ptr, x.data_ptr(), H, code, int(bool(zero_pad)), recv_x.data_ptr(),
+    recv_x, recv_scales = _dispatch_outputs(H, out_dtype, recv_x, recv_scales, capacity, x.device,
+                                            scales_col_major)
+    _check_dispatch(x, recv_x, recv_scales, out_dtype, scales_col_major)
+    _check(_lib().ep_dispatch(handle.ptr, x.data_ptr(), xcode,
+                              x_scales.data_ptr() if x_scales is not None else None, H, code,
+                              _flags(zero_pad, scales_col_major), recv_x.data_ptr(),
                               recv_scales.data_ptr() if recv_scales is not None else None,
                               recv_x.shape[0], _stream_ptr(stream)), "ep_dispatch")
     return recv_x, recv_scales
@@ -291,15 +331,19 @@ def dispatch(handle: EPHandle, x: torch.Tensor, out_dtype: str = "bf16", zero_pa
 def dispatch_cached(handle: EPHandle, x: torch.Tensor, num_experts: int, expert_alignment: int,
                     num_tokens_per_rank: int, out_dtype: str = "bf16", zero_pad: bool = True,
                     recv_x: Optional[torch.Tensor] = None, recv_scales: Optional[torch.Tensor] = None,
-                    stream: Optional[torch.cuda.Stream] = None):
+                    stream: Optional[torch.cuda.Stream] = None, x_scales: Optional[torch.Tensor] = None,
+                    scales_col_major: bool = False):
     """Cached-handle dispatch: checks (E, A, S) against the handle first."""
     code = _dtype_code(out_dtype)
+    xcode = _input_code(x, x_scales)
     H = x.shape[1]
     capacity = handle.sizes(stream)[0] if recv_x is None else None
-    recv_x, recv_scales = _dispatch_outputs(H, out_dtype, recv_x, recv_scales, capacity, x.device)
-    _check_dispatch(x, recv_x, recv_scales, out_dtype)
+    recv_x, recv_scales = _dispatch_outputs(H, out_dtype, recv_x, recv_scales, capacity, x.device,
+                                            scales_col_major)
+    _check_dispatch(x, recv_x, recv_scales, out_dtype, scales_col_major)
     _check(_lib().ep_dispatch_cached(handle.ptr, num_experts, expert_alignment, num_tokens_per_rank,
-                                     x.data_ptr(), H, code, int(bool(zero_pad)), recv_x.data_ptr(),
+                                     x.data_ptr(), xcode, x_scales.data_ptr() if x_scales is not None else None,
+                                     H, code, _flags(zero_pad, scales_col_major), recv_x.data_ptr(),
                                      recv_scales.data_ptr() if recv_scales is not None else None,
                                      recv_x.shape[0], _stream_ptr(stream)), "ep_dispatch_cached")
     return recv_x, recv_scales
@@ -309,30 +353,62 @@ def dispatch_fresh(topk_idx: torch.Tensor, x: torch.Tensor, num_ranks: int, num_
                    expert_alignment: int = 1, num_channels: int = 0, out_dtype: str = "bf16",
                    zero_pad: bool = True, recv_x: Optional[torch.Tensor] = None,
                    recv_scales: Optional[torch.Tensor] = None,
-                   stream: Optional[torch.cuda.Stream] = None):
+                   stream: Optional[torch.cuda.Stream] = None, x_scales: Optional[torch.Tensor] = None,
+                   scales_col_major: bool = False):
     """Plan + dispatch in one library call; outputs default to the worst-case
     row count (no synchronisation).  Returns (handle, recv_x, recv_scales)."""
     _need(topk_idx, "topk_idx", torch.int64, 2)
     code = _dtype_code(out_dtype)
+    xcode = _input_code(x, x_scales)
     T, K = topk_idx.shape
     H = x.shape[1]
     cap = worst_expanded_rows(T, K, num_experts, expert_alignment)
-    recv_x, recv_scales = _dispatch_outputs(H, out_dtype, recv_x, recv_scales, cap, x.device)
-    _check_dispatch(x, recv_x, recv_scales, out_dtype)
+    recv_x, recv_scales = _dispatch_outputs(H, out_dtype, recv_x, recv_scales, cap, x.device, scales_col_major)
+    _check_dispatch(x, recv_x, recv_scales, out_dtype, scales_col_major)
     h = ctypes.c_void_p()
     _check(_lib().ep_dispatch_fresh(topk_idx.data_ptr(), T // num_ranks, num_ranks, K, num_experts,
-                                    expert_alignment, num_channels, x.data_ptr(), H, code,
-                                    int(bool(zero_pad)), recv_x.data_ptr(),
+                                    expert_alignment, num_channels, x.data_ptr(), xcode,
+                                    x_scales.data_ptr() if x_scales is not None else None, H, code,
+                                    _flags(zero_pad, scales_col_major), recv_x.data_ptr(),
                                     recv_scales.data_ptr() if recv_scales is not None else None,
                                     recv_x.shape[0], _stream_ptr(stream), ctypes.byref(h)),
            "ep_dispatch_fresh")
     return EPHandle(h.value, stream), recv_x, recv_scales
 
 
+def dispatch_metadata(handle: EPHandle, topk_weights: torch.Tensor, capacity: Optional[int] = None,
+                      recv_weights: Optional[torch.Tensor] = None, recv_meta: Optional[torch.Tensor] = None,
+                      zero_pad: bool = True, stream: Optional[torch.cuda.Stream] = None):
+    """Per expanded row: (routing weight [rows] f32, {source token, slot k} [rows,2] i32)."""
+    _need(topk_weights, "topk_weights", torch.float32, 2)
+    if tuple(topk_weights.shape) != (handle.T, handle.K):
+        raise ValueError("topk_weights must be [T,K]")
+    if capacity is None:
+        capacity = recv_weights.shape[0] if recv_weights is not None else handle.sizes(stream)[0]
+    if recv_weights is None:
+        recv_weights = torch.empty(capacity, dtype=torch.float32, device=topk_weights.device)
+    if recv_meta is None:
+        recv_meta = torch.empty((capacity, 2), dtype=torch.int32, device=topk_weights.device)
+    _need(recv_weights, "recv_weights", torch.float32, 1)
+    _need(recv_meta, "recv_meta", torch.int32, 2)
+    if recv_weights.shape[0] < capacity or recv_meta.shape[0] < capacity:
+        raise ValueError("output buffers smaller than capacity")
+    _check(_lib().ep_dispatch_metadata(handle.ptr, topk_weights.data_ptr(), recv_weights.data_ptr(),
+                                       recv_meta.data_ptr(), capacity, int(bool(zero_pad)), _stream_ptr(stream)),
+           "ep_dispatch_metadata")
+    return recv_weights, recv_meta
+
+
 def combine(handle: EPHandle, y: torch.Tensor, topk_weights: torch.Tensor,
-            out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
-    """Weighted combine of y [rows,H] bf16 back to [T,H] bf16."""
+            out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+            bias: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Weighted combine of y [rows,H] bf16 back to [T,H] bf16, plus an
+    optional bias row [T,H] bf16 added before the rounding."""
     _need(y, "y", torch.bfloat16, 2)
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, 2)
+        if tuple(bias.shape) != (handle.T, y.shape[1]):
+            raise ValueError("bias must be [T,H]")
     _need(topk_weights, "topk_weights", torch.float32, 2)
     if tuple(topk_weights.shape) != (handle.T, handle.K):
         raise ValueError("topk_weights must be [T,K]")
@@ -342,8 +418,9 @@ def combine(handle: EPHandle, y: torch.Tensor, topk_weights: torch.Tensor,
     _need(out, "out", torch.bfloat16, 2)
     if tuple(out.shape) != (handle.T, H):
         raise ValueError("out must be [T,H]")
-    _check(_lib().ep_combine(handle.ptr, y.data_ptr(), y.shape[0], topk_weights.data_ptr(), H,
-                             out.data_ptr(), _stream_ptr(stream)), "ep_combine")
+    _check(_lib().ep_combine(handle.ptr, y.data_ptr(), y.shape[0], topk_weights.data_ptr(),
+                             bias.data_ptr() if bias is not None else None, H, out.data_ptr(),
+                             _stream_ptr(stream)), "ep_combine")
     return out
 
 

@@ -19,7 +19,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 1;
+constexpr int kAbiVersion = 2;
 constexpr long long kDefaultPollLimit = 1ll << 20;
 
 long long g_poll_limit = kDefaultPollLimit;
@@ -195,14 +195,26 @@ ep_status_t read_status_word(ep_handle_s* h, cudaStream_t stream, bool clear, in
   return EP_OK;
 }
 
-ep_status_t check_dispatch_args(ep_handle_s* h, const void* x, int64_t H, ep_dtype_t out_dtype,
-                                void* recv_x, float* recv_scales, int64_t capacity) {
+ep_status_t check_dispatch_args(ep_handle_s* h, const void* x, ep_dtype_t x_dtype, const float* x_scales,
+                                int64_t H, ep_dtype_t out_dtype, int flags, void* recv_x, float* recv_scales,
+                                int64_t capacity) {
   if (!h || !x || !recv_x || capacity < 0 || H < 8 || H % 8 != 0) return EP_ERR_INVALID;
+  if ((flags & ~(EP_DISPATCH_ZERO_PAD | EP_DISPATCH_SCALES_COL_MAJOR)) != 0) return EP_ERR_INVALID;
   if (!aligned(x, 16) || !aligned(recv_x, 16)) return EP_ERR_INVALID;
-  if (out_dtype == EP_DTYPE_BF16) {
-    if (recv_scales) return EP_ERR_INVALID;
-  } else if (out_dtype == EP_DTYPE_FP8_E4M3) {
-    if (H % 128 != 0 || !recv_scales || !aligned(recv_scales, 16)) return EP_ERR_INVALID;
+  if (x_dtype == EP_DTYPE_BF16) {
+    if (x_scales) return EP_ERR_INVALID;
+    if (out_dtype == EP_DTYPE_BF16) {
+      if (recv_scales || (flags & EP_DISPATCH_SCALES_COL_MAJOR)) return EP_ERR_INVALID;
+    } else if (out_dtype == EP_DTYPE_FP8_E4M3) {
+      if (H % 128 != 0 || !recv_scales || !aligned(recv_scales, 16)) return EP_ERR_INVALID;
+    } else {
+      return EP_ERR_INVALID;
+    }
+  } else if (x_dtype == EP_DTYPE_FP8_E4M3) {
+    // pre-quantised input is passed through: codes and scales
+    if (out_dtype != EP_DTYPE_FP8_E4M3 || H % 128 != 0 || !x_scales || !aligned(x_scales, 4) ||
+        !recv_scales || !aligned(recv_scales, 4))
+      return EP_ERR_INVALID;
   } else {
     return EP_ERR_INVALID;
   }
@@ -290,13 +302,16 @@ int64_t ep_worst_expanded_rows(int64_t T, int K, int E, int A) {
   return T * K + static_cast<int64_t>(E) * (A - 1);
 }
 
-ep_status_t ep_dispatch(ep_handle_t h, const void* x, int64_t H, ep_dtype_t out_dtype, int zero_pad,
-                        void* recv_x, float* recv_scales, int64_t capacity, ep_stream_t stream_) {
-  ep_status_t st = check_dispatch_args(h, x, H, out_dtype, recv_x, recv_scales, capacity);
+ep_status_t ep_dispatch(ep_handle_t h, const void* x, ep_dtype_t x_dtype, const float* x_scales, int64_t H,
+                        ep_dtype_t out_dtype, int flags, void* recv_x, float* recv_scales, int64_t capacity,
+                        ep_stream_t stream_) {
+  ep_status_t st = check_dispatch_args(h, x, x_dtype, x_scales, H, out_dtype, flags, recv_x, recv_scales, capacity);
   if (st != EP_OK) return st;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  const bool zero_pad = (flags & EP_DISPATCH_ZERO_PAD) != 0;
   ep::DispatchDev d;
   d.x = x;
+  d.x_scales = x_scales;
   d.slot = h->dev.slot;
   d.pad_rows = h->dev.pad_rows;
   d.sizes = h->dev.sizes;
@@ -309,38 +324,41 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, int64_t H, ep_dtype_t out_
   d.capacity = capacity;
   d.max_pad = zero_pad ? h->cap_pad : 0;
   d.zero_pad = zero_pad ? 1 : 0;
-  cudaError_t e = out_dtype == EP_DTYPE_BF16 ? ep::launch_dispatch_bf16(d, stream)
-                                              : ep::launch_dispatch_fp8(d, stream);
+  d.scales_col_major = (flags & EP_DISPATCH_SCALES_COL_MAJOR) ? 1 : 0;
+  cudaError_t e;
+  if (x_dtype == EP_DTYPE_FP8_E4M3)
+    e = ep::launch_dispatch_fp8_input(d, stream);
+  else if (out_dtype == EP_DTYPE_BF16)
+    e = ep::launch_dispatch_bf16(d, stream);
+  else
+    e = ep::launch_dispatch_fp8(d, stream);
   return cuda_status(e);
 }
 
-ep_status_t ep_dispatch_cached(ep_handle_t h, int E, int A, int64_t S, const void* x, int64_t H,
-                               ep_dtype_t out_dtype, int zero_pad, void* recv_x, float* recv_scales,
-                               int64_t capacity, ep_stream_t stream) {
+ep_status_t ep_dispatch_cached(ep_handle_t h, int E, int A, int64_t S, const void* x, ep_dtype_t x_dtype,
+                               const float* x_scales, int64_t H, ep_dtype_t out_dtype, int flags, void* recv_x,
+                               float* recv_scales, int64_t capacity, ep_stream_t stream) {
   if (!h) return EP_ERR_INVALID;
   if (h->dev.E != E || h->dev.A != A || h->dev.S != S) return EP_ERR_MISMATCH;
-  return ep_dispatch(h, x, H, out_dtype, zero_pad, recv_x, recv_scales, capacity, stream);
+  return ep_dispatch(h, x, x_dtype, x_scales, H, out_dtype, flags, recv_x, recv_scales, capacity, stream);
 }
 
 ep_status_t ep_dispatch_fresh(const int64_t* topk_idx, int64_t S, int P, int K, int E, int A, int C,
-                              const void* x, int64_t H, ep_dtype_t out_dtype, int zero_pad,
-                              void* recv_x, float* recv_scales, int64_t capacity,
-                              ep_stream_t stream, ep_handle_t* out) {
+                              const void* x, ep_dtype_t x_dtype, const float* x_scales, int64_t H,
+                              ep_dtype_t out_dtype, int flags, void* recv_x, float* recv_scales,
+                              int64_t capacity, ep_stream_t stream, ep_handle_t* out) {
   if (!out) return EP_ERR_INVALID;
   *out = nullptr;
   // Check the dispatch arguments before planning so that nothing is enqueued
-  // for a call that cannot run.
-  if (!x || !recv_x || capacity < 0 || H < 8 || H % 8 != 0 || !aligned(x, 16) ||
-      !aligned(recv_x, 16))
-    return EP_ERR_INVALID;
-  if (out_dtype == EP_DTYPE_FP8_E4M3 && (H % 128 != 0 || !recv_scales || !aligned(recv_scales, 16)))
-    return EP_ERR_INVALID;
-  if (out_dtype == EP_DTYPE_BF16 && recv_scales) return EP_ERR_INVALID;
-  if (out_dtype != EP_DTYPE_BF16 && out_dtype != EP_DTYPE_FP8_E4M3) return EP_ERR_INVALID;
-  ep_handle_t h = nullptr;
-  ep_status_t st = ep_plan(topk_idx, S, P, K, E, A, C, stream, &h);
+  // for a call that cannot run (a dummy handle pointer stands in for the plan).
+  ep_handle_s probe;
+  ep_status_t st = check_dispatch_args(&probe, x, x_dtype, x_scales, H, out_dtype, flags, recv_x, recv_scales,
+                                       capacity);
   if (st != EP_OK) return st;
-  st = ep_dispatch(h, x, H, out_dtype, zero_pad, recv_x, recv_scales, capacity, stream);
+  ep_handle_t h = nullptr;
+  st = ep_plan(topk_idx, S, P, K, E, A, C, stream, &h);
+  if (st != EP_OK) return st;
+  st = ep_dispatch(h, x, x_dtype, x_scales, H, out_dtype, flags, recv_x, recv_scales, capacity, stream);
   if (st != EP_OK) {
     ep_handle_destroy(h, stream);
     return st;
@@ -349,12 +367,33 @@ ep_status_t ep_dispatch_fresh(const int64_t* topk_idx, int64_t S, int P, int K, 
   return EP_OK;
 }
 
-ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, const float* w, int64_t H,
-                       void* out, ep_stream_t stream) {
+ep_status_t ep_dispatch_metadata(ep_handle_t h, const float* w, float* recv_weights, int32_t* recv_meta,
+                                 int64_t capacity, int zero_pad, ep_stream_t stream) {
+  if (!h || !w || !recv_weights || !recv_meta || capacity < 0) return EP_ERR_INVALID;
+  if (!aligned(w, 4) || !aligned(recv_weights, 4) || !aligned(recv_meta, 4)) return EP_ERR_INVALID;
+  ep::MetaDev m;
+  m.slot = h->dev.slot;
+  m.weights = w;
+  m.pad_rows = h->dev.pad_rows;
+  m.sizes = h->dev.sizes;
+  m.status = h->dev.ctr + ep::kCtrStatus;
+  m.recv_weights = recv_weights;
+  m.recv_meta = recv_meta;
+  m.T = h->dev.T;
+  m.K = h->dev.K;
+  m.capacity = capacity;
+  m.max_pad = zero_pad ? h->cap_pad : 0;
+  return cuda_status(ep::launch_dispatch_metadata(m, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, const float* w, const void* bias,
+                       int64_t H, void* out, ep_stream_t stream) {
   if (!h || !y || !w || !out || y_rows < 0 || H < 8 || H % 8 != 0) return EP_ERR_INVALID;
-  if (!aligned(y, 16) || !aligned(out, 16) || !aligned(w, 4)) return EP_ERR_INVALID;
+  if (!aligned(y, 16) || !aligned(out, 16) || !aligned(w, 4) || (bias && !aligned(bias, 16)))
+    return EP_ERR_INVALID;
   ep::CombineDev c;
   c.y = y;
+  c.bias = bias;
   c.slot = h->dev.slot;
   c.weights = w;
   c.status = h->dev.ctr + ep::kCtrStatus;
@@ -372,6 +411,7 @@ ep_status_t ep_dispatch_backward(ep_handle_t h, const void* grad_recv, int64_t g
   if (!aligned(grad_recv, 16) || !aligned(grad_x, 16)) return EP_ERR_INVALID;
   ep::CombineDev c;
   c.y = grad_recv;
+  c.bias = nullptr;
   c.slot = h->dev.slot;
   c.weights = nullptr;  // unit weights: the sum over the token's expanded rows
   c.status = h->dev.ctr + ep::kCtrStatus;

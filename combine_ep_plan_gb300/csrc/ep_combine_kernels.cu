@@ -71,6 +71,14 @@ __global__ void __launch_bounds__(256, MINB) ep_combine_kernel(CombineDev c) {
         if (row[k] >= 0 && v < hv) buf[k][u] = ld_stream(src + v);
       }
     }
+    uint4 bv[U];
+    if (c.bias) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t v = v0 + u * 32 + lane;
+        if (v < hv) bv[u] = ld_stream(static_cast<const uint4*>(c.bias) + g * hv + v);
+      }
+    }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t v = v0 + u * 32 + lane;
@@ -86,6 +94,14 @@ __global__ void __launch_bounds__(256, MINB) ep_combine_kernel(CombineDev c) {
         for (int i = 0; i < 4; ++i) {
           acc[2 * i] = fmaf(wk[k], __uint_as_float(wv[i] << 16), acc[2 * i]);
           acc[2 * i + 1] = fmaf(wk[k], __uint_as_float(wv[i] & 0xffff0000u), acc[2 * i + 1]);
+        }
+      }
+      if (c.bias) {  // the fused residual / shared-expert row, added once in fp32
+        const unsigned bw[4] = {bv[u].x, bv[u].y, bv[u].z, bv[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] = __fadd_rn(acc[2 * i], __uint_as_float(bw[i] << 16));
+          acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __uint_as_float(bw[i] & 0xffff0000u));
         }
       }
       uint4 o;

@@ -35,11 +35,21 @@ constexpr int kUnroll = 4;
 // Work item = (row item, column chunk of 32*kUnroll vectors): T token rows
 // then N_pad padding rows, each cut into chunks, so that every warp gets many
 // small items and the kernel has no long tail.
-__global__ void __launch_bounds__(256) ep_dispatch_bf16_kernel(DispatchDev a) {
+// Scale index of group j of expanded row r, in the requested layout.
+__device__ __forceinline__ int64_t scale_at(const DispatchDev& a, int64_t r, int64_t j, int64_t groups) {
+  return a.scales_col_major ? j * a.capacity + r : r * groups + j;
+}
+
+// Copies whole rows: BF16 hidden rows (row_vec = H/8 vectors), or E4M3 codes
+// of pre-quantised input (row_vec = H/16) together with their H/128 fp32
+// scales, which the warp owning chunk 0 of a row copies.
+template <int ROW_DIV, bool WITH_SCALES>
+__global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-  const int64_t hv = a.H / 8;  // 16-byte vectors per row
+  const int64_t hv = a.H / ROW_DIV;  // 16-byte vectors per row
+  const int64_t groups = a.H / 128;
   constexpr int kChunk = 32 * kUnroll;
   const int64_t chunks = (hv + kChunk - 1) / kChunk;
   const int64_t n_pad = a.zero_pad ? a.sizes[kSizePad] : 0;
@@ -65,6 +75,7 @@ __global__ void __launch_bounds__(256) ep_dispatch_bf16_kernel(DispatchDev a) {
         const int64_t v = v0 + u * 32 + lane;
         if (v < hv) buf[u] = ld_stream(src + v);
       }
+      const bool copy_scales = WITH_SCALES && v0 == 0;
       for (int k = 0; k < a.K; ++k) {
         const int r = __shfl_sync(0xffffffffu, my_row, k);
         if (r < 0) continue;
@@ -74,6 +85,8 @@ __global__ void __launch_bounds__(256) ep_dispatch_bf16_kernel(DispatchDev a) {
           const int64_t v = v0 + u * 32 + lane;
           if (v < hv) st_row(dst + v, buf[u]);
         }
+        if (copy_scales)
+          for (int64_t j = lane; j < groups; j += 32) a.scales[scale_at(a, r, j, groups)] = a.x_scales[g * groups + j];
       }
     } else {
       const int r = a.pad_rows[ri - a.T];
@@ -88,6 +101,8 @@ __global__ void __launch_bounds__(256) ep_dispatch_bf16_kernel(DispatchDev a) {
         const int64_t v = v0 + u * 32 + lane;
         if (v < hv) st_row(dst + v, z);
       }
+      if (WITH_SCALES && v0 == 0)
+        for (int64_t j = lane; j < groups; j += 32) a.scales[scale_at(a, r, j, groups)] = 0.0f;
     }
   }
 }
@@ -231,7 +246,7 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
           const int64_t qi = q_base + u * kUnitVec + lane;
           if (qi < qv) st_row(dst + qi, q[u]);
         }
-        if (sc_active) a.scales[static_cast<int64_t>(r) * groups + g_base + lane] = my_scale;
+        if (sc_active) a.scales[scale_at(a, r, g_base + lane, groups)] = my_scale;
       }
     } else {
       const int r = a.pad_rows[ri - a.T];
@@ -245,7 +260,7 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
         const int64_t qi = q_base + u * kUnitVec + lane;
         if (qi < qv) st_row(dst + qi, make_uint4(0u, 0u, 0u, 0u));
       }
-      if (sc_active) a.scales[static_cast<int64_t>(r) * groups + g_base + lane] = 0.0f;
+      if (sc_active) a.scales[scale_at(a, r, g_base + lane, groups)] = 0.0f;
     }
   }
 }
@@ -264,7 +279,52 @@ unsigned item_grid(int64_t rows, int64_t chunks) {
 
 cudaError_t launch_dispatch_bf16(const DispatchDev& d, cudaStream_t stream) {
   const int64_t chunks = (d.H / 8 + 32 * kUnroll - 1) / (32 * kUnroll);
-  ep_dispatch_bf16_kernel<<<item_grid(d.T + d.max_pad, chunks), 256, 0, stream>>>(d);
+  ep_dispatch_copy_kernel<8, false><<<item_grid(d.T + d.max_pad, chunks), 256, 0, stream>>>(d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_fp8_input(const DispatchDev& d, cudaStream_t stream) {
+  const int64_t chunks = (d.H / 16 + 32 * kUnroll - 1) / (32 * kUnroll);
+  ep_dispatch_copy_kernel<16, true><<<item_grid(d.T + d.max_pad, chunks), 256, 0, stream>>>(d);
+  return cudaGetLastError();
+}
+
+namespace {
+
+// Per expanded row: the routing weight and {source token, slot k}; one
+// thread per (token, slot), then one per padding row.
+__global__ void __launch_bounds__(256) ep_dispatch_metadata_kernel(MetaDev m) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t pairs = m.T * m.K;
+  if (i < pairs) {
+    const int r = m.slot[i];
+    if (r < 0) return;
+    if (r >= m.capacity) {
+      atomicOr(m.status, kStCapacity);
+      return;
+    }
+    m.recv_weights[r] = m.weights[i];
+    m.recv_meta[2 * static_cast<int64_t>(r)] = static_cast<int>(i / m.K);
+    m.recv_meta[2 * static_cast<int64_t>(r) + 1] = static_cast<int>(i % m.K);
+    return;
+  }
+  const int64_t pi = i - pairs;
+  if (pi >= m.sizes[kSizePad]) return;
+  const int r = m.pad_rows[pi];
+  if (r >= m.capacity) {
+    atomicOr(m.status, kStCapacity);
+    return;
+  }
+  m.recv_weights[r] = 0.0f;
+  m.recv_meta[2 * static_cast<int64_t>(r)] = -1;
+  m.recv_meta[2 * static_cast<int64_t>(r) + 1] = -1;
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_metadata(const MetaDev& m, cudaStream_t stream) {
+  const int64_t n = m.T * m.K + m.max_pad;
+  ep_dispatch_metadata_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(m);
   return cudaGetLastError();
 }
 

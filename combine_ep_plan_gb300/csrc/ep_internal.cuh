@@ -77,7 +77,8 @@ cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream);
 size_t plan_smem_bytes(int P, int E, int K);
 
 struct DispatchDev {
-  const void* x;          // [T,H] bf16
+  const void* x;          // [T,H] bf16, or [T,H] E4M3 codes (pre-quantised input)
+  const float* x_scales;  // [T,H/128] scales of pre-quantised input, else NULL
   const int* slot;        // [T,K]
   const int* pad_rows;    // [N_pad]
   const int* sizes;       // device sizes (N_pad read on device)
@@ -90,12 +91,30 @@ struct DispatchDev {
   int64_t capacity;
   int64_t max_pad;        // upper bound of N_pad: E*(A-1) (sizes the grid)
   int zero_pad;
+  int scales_col_major;   // scales stored [H/128][capacity] instead of [capacity][H/128]
 };
 cudaError_t launch_dispatch_bf16(const DispatchDev& d, cudaStream_t stream);
 cudaError_t launch_dispatch_fp8(const DispatchDev& d, cudaStream_t stream);
+cudaError_t launch_dispatch_fp8_input(const DispatchDev& d, cudaStream_t stream);
+
+struct MetaDev {
+  const int* slot;        // [T,K]
+  const float* weights;   // [T,K]
+  const int* pad_rows;    // [N_pad]
+  const int* sizes;
+  unsigned* status;
+  float* recv_weights;    // [capacity]
+  int* recv_meta;         // [capacity,2]
+  int64_t T;
+  int K;
+  int64_t capacity;
+  int64_t max_pad;
+};
+cudaError_t launch_dispatch_metadata(const MetaDev& m, cudaStream_t stream);
 
 struct CombineDev {
   const void* y;          // [y_rows,H] bf16
+  const void* bias;       // [T,H] bf16 added after the weighted sum, or NULL
   const int* slot;        // [T,K]
   const float* weights;   // [T,K]; NULL: unit weights (the dispatch backward)
   unsigned* status;

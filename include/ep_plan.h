@@ -56,6 +56,10 @@ typedef enum {
     EP_DTYPE_FP8_E4M3 = 1  /* OCP E4M3 ("fn"), 1 byte, with fp32 scales per 128 */
 } ep_dtype_t;
 
+/* Flags of the dispatch entry points. */
+#define EP_DISPATCH_ZERO_PAD 1          /* zero the padding rows (codes and scales) */
+#define EP_DISPATCH_SCALES_COL_MAJOR 2  /* FP8 scales stored [H/128][capacity_rows] */
+
 /* Limits of this implementation (checked; EP_ERR_INVALID beyond them). */
 #define EP_MAX_RANKS 1024
 #define EP_MAX_EXPERTS 2048
@@ -147,26 +151,38 @@ int64_t ep_worst_expanded_rows(int64_t num_tokens, int num_topk, int num_experts
  * written to every expanded row of its (token, slot) pairs, which groups rows
  * by expert and pads each segment to A rows ([TT] §2.2, §4.3 local copy).
  *
- * x_dev          [T,H] bfloat16, 16-byte aligned, H % 8 == 0.
+ * x_dev          [T,H], 16-byte aligned, H % 8 == 0: bfloat16 (x_dtype
+ *                EP_DTYPE_BF16), or E4M3 codes already quantised with fp32
+ *                scales per 128 elements (x_dtype EP_DTYPE_FP8_E4M3, [TT]
+ *                §3.6: x arrives as (codes, scales)).
+ * x_scales_dev   [T,H/128] fp32 row-major scales of pre-quantised input;
+ *                NULL for bfloat16 input.
  * hidden         H.
- * out_dtype      EP_DTYPE_BF16: recv_x is [capacity_rows,H] bfloat16, a bit copy.
- *                EP_DTYPE_FP8_E4M3: quantised inside dispatch ([TT] §3.6):
- *                per row and per 128 elements, scale = amax/448 (IEEE fp32
- *                division), code = E4M3(x/scale) rounded to nearest even with
- *                saturation; amax == 0 gives scale 0 and zero codes.  recv_x is
- *                [capacity_rows,H] E4M3 bytes, recv_scales_dev [capacity_rows,H/128]
- *                fp32 row-major.  Needs H % 128 == 0.
- * zero_pad       nonzero: padding rows are zero (codes and scales); 0: padding
- *                rows are left untouched ([TT] §2.2, do_zero_padding).
+ * out_dtype      EP_DTYPE_BF16 (bfloat16 input only): recv_x is
+ *                [capacity_rows,H] bfloat16, a bit copy.
+ *                EP_DTYPE_FP8_E4M3: recv_x is [capacity_rows,H] E4M3 codes and
+ *                recv_scales_dev holds H/128 fp32 scales per row.  From
+ *                bfloat16 input the rows are quantised inside dispatch ([TT]
+ *                §3.6): per row and per 128 elements, scale = amax/448 (IEEE
+ *                fp32 division), code = E4M3(x/scale) rounded to nearest even
+ *                with saturation; amax == 0 gives scale 0 and zero codes.  From
+ *                pre-quantised input codes and scales are copied.  Needs
+ *                H % 128 == 0.
+ * flags          EP_DISPATCH_ZERO_PAD: padding rows are zero (codes and
+ *                scales), otherwise untouched ([TT] §2.2, do_zero_padding).
+ *                EP_DISPATCH_SCALES_COL_MAJOR: scale j of row r is stored at
+ *                recv_scales[j*capacity_rows + r] (the column-major layout of
+ *                [TT] §3.6, stride (1, rows) for a [rows, H/128] view) instead
+ *                of recv_scales[r*(H/128) + j].
  * recv_x_dev     output, 16-byte aligned.  Rows >= N_exp are never written.
- * recv_scales_dev output for FP8, 16-byte aligned; must be NULL for BF16.
+ * recv_scales_dev output for FP8; must be NULL for BF16 output.
  * capacity_rows  rows available in recv_x (and recv_scales).  A capacity below
  *                N_exp records EP_ERR_CAPACITY and writes no row at or beyond it.
  * Reusing a handle on new x is the cached dispatch of [TT] §2.4: no plan work.
  */
-ep_status_t ep_dispatch(ep_handle_t handle, const void *x_dev, int64_t hidden,
-                        ep_dtype_t out_dtype, int zero_pad, void *recv_x_dev,
-                        float *recv_scales_dev, int64_t capacity_rows,
+ep_status_t ep_dispatch(ep_handle_t handle, const void *x_dev, ep_dtype_t x_dtype,
+                        const float *x_scales_dev, int64_t hidden, ep_dtype_t out_dtype, int flags,
+                        void *recv_x_dev, float *recv_scales_dev, int64_t capacity_rows,
                         ep_stream_t stream);
 
 /*
@@ -176,24 +192,39 @@ ep_status_t ep_dispatch(ep_handle_t handle, const void *x_dev, int64_t hidden,
  * A difference returns EP_ERR_MISMATCH and enqueues nothing.
  */
 ep_status_t ep_dispatch_cached(ep_handle_t handle, int num_experts, int expert_alignment,
-                               int64_t num_tokens_per_rank, const void *x_dev,
-                               int64_t hidden, ep_dtype_t out_dtype, int zero_pad,
-                               void *recv_x_dev, float *recv_scales_dev,
+                               int64_t num_tokens_per_rank, const void *x_dev, ep_dtype_t x_dtype,
+                               const float *x_scales_dev, int64_t hidden, ep_dtype_t out_dtype,
+                               int flags, void *recv_x_dev, float *recv_scales_dev,
                                int64_t capacity_rows, ep_stream_t stream);
 
 /*
  * ep_dispatch_fresh — ep_plan followed by ep_dispatch in one call (a fresh
  * dispatch that re-plans the routing, [DO] "Fresh dispatch 是什么意思").  On
  * success *out_handle_host holds the new plan for later cached dispatches and
- * combines.  Arguments as for ep_plan and ep_dispatch.
+ * combines.  Arguments as for ep_plan and ep_dispatch; invalid dispatch
+ * arguments are rejected before the plan is enqueued.
  */
 ep_status_t ep_dispatch_fresh(const int64_t *topk_idx_dev, int64_t num_tokens_per_rank,
                               int num_ranks, int num_topk, int num_experts,
                               int expert_alignment, int num_channels, const void *x_dev,
-                              int64_t hidden, ep_dtype_t out_dtype, int zero_pad,
-                              void *recv_x_dev, float *recv_scales_dev,
-                              int64_t capacity_rows, ep_stream_t stream,
+                              ep_dtype_t x_dtype, const float *x_scales_dev, int64_t hidden,
+                              ep_dtype_t out_dtype, int flags, void *recv_x_dev,
+                              float *recv_scales_dev, int64_t capacity_rows, ep_stream_t stream,
                               ep_handle_t *out_handle_host);
+
+/*
+ * ep_dispatch_metadata — the metadata that travels with each dispatched row
+ * ([TT] §2.1 and §4.2: the routing weight and the source token): for every
+ * expanded row r = slot[g,k], recv_weights[r] = topk_weights[g,k] and
+ * recv_meta[r] = {g, k}.  With zero_pad, padding rows get weight 0 and
+ * {-1, -1}; otherwise they are untouched.
+ * topk_weights_dev [T,K] float32; recv_weights_dev [capacity_rows] float32;
+ * recv_meta_dev [capacity_rows,2] int32.  A row at or beyond capacity_rows
+ * records EP_ERR_CAPACITY and is not written.
+ */
+ep_status_t ep_dispatch_metadata(ep_handle_t handle, const float *topk_weights_dev,
+                                 float *recv_weights_dev, int32_t *recv_meta_dev,
+                                 int64_t capacity_rows, int zero_pad, ep_stream_t stream);
 
 /*
  * ep_combine — the inverse of dispatch ([TT] §2.3): gather each token's
@@ -201,17 +232,20 @@ ep_status_t ep_dispatch_fresh(const int64_t *topk_idx_dev, int64_t num_tokens_pe
  * out[g,:] = bf16_RNE( sum over k = 0..K-1 with slot[g,k] >= 0, in that
  * order, of fmaf(w[g,k], float(y[slot[g,k],:]), acc) ), acc starting at 0;
  * fp32 accumulation, rounded once ([TT] §4.5).  A token with no valid slot
- * gives zeros.  Padding rows of y are never read.
+ * gives zeros.  Padding rows of y are never read.  With a bias row (the
+ * fused residual or shared-expert output of [TT] §3.3) the sum is
+ * acc + float(bias[g,:]) before the rounding.
  *
  * y_dev          [y_rows,H] bfloat16 expert outputs in the expanded layout,
  *                16-byte aligned, H % 8 == 0.  y_rows < N_exp records
  *                EP_ERR_CAPACITY (rows beyond y_rows are not read).
  * topk_weights_dev [T,K] float32.
+ * bias_dev       [T,H] bfloat16, 16-byte aligned, or NULL.
  * out_dev        [T,H] bfloat16, 16-byte aligned.
  */
 ep_status_t ep_combine(ep_handle_t handle, const void *y_dev, int64_t y_rows,
-                       const float *topk_weights_dev, int64_t hidden, void *out_dev,
-                       ep_stream_t stream);
+                       const float *topk_weights_dev, const void *bias_dev, int64_t hidden,
+                       void *out_dev, ep_stream_t stream);
 
 /*
  * ep_dispatch_backward — the backward of dispatch, which is a combine on the

@@ -41,7 +41,7 @@ def test_header_declares_the_boundary():
 def test_every_declared_symbol_is_exported(lib):
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
-    assert lib.ep_abi_version() == 1
+    assert lib.ep_abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -85,17 +85,26 @@ def test_plan_rejects_null_and_misaligned(lib):
 
 
 def test_calls_on_null_handle_are_rejected(lib):
-    assert lib.ep_dispatch(None, FAKE, 256, 0, 1, FAKE, None, 10, None) == ep.EP_ERR_INVALID
-    assert lib.ep_combine(None, FAKE, 10, FAKE, 256, FAKE, None) == ep.EP_ERR_INVALID
+    assert lib.ep_dispatch(None, FAKE, 0, None, 256, 0, 1, FAKE, None, 10, None) == ep.EP_ERR_INVALID
+    assert lib.ep_combine(None, FAKE, 10, FAKE, None, 256, FAKE, None) == ep.EP_ERR_INVALID
+    assert lib.ep_dispatch_metadata(None, FAKE, FAKE, FAKE, 10, 1, None) == ep.EP_ERR_INVALID
     assert lib.ep_sync_status(None, None) == ep.EP_ERR_INVALID
     assert lib.ep_handle_destroy(None, None) == ep.EP_ERR_INVALID
-    assert lib.ep_dispatch_cached(None, 8, 1, 64, FAKE, 256, 0, 1, FAKE, None, 10, None) == ep.EP_ERR_INVALID
+    assert lib.ep_dispatch_cached(None, 8, 1, 64, FAKE, 0, None, 256, 0, 1, FAKE, None, 10, None) == \
+        ep.EP_ERR_INVALID
     h = ctypes.c_void_p()
-    # fresh dispatch: bad hidden size / misaligned output rejected before planning
-    assert lib.ep_dispatch_fresh(FAKE, 64, 4, 2, 8, 1, 0, FAKE, 100, 0, 1, FAKE, None, 10, None,
-                                 ctypes.byref(h)) == ep.EP_ERR_INVALID
-    assert lib.ep_dispatch_fresh(FAKE, 64, 4, 2, 8, 1, 0, FAKE, 256, 0, 1, FAKE + 8, None, 10, None,
-                                 ctypes.byref(h)) == ep.EP_ERR_INVALID
-    assert lib.ep_dispatch_fresh(FAKE, 64, 4, 2, 8, 1, 0, FAKE, 200, 1, 1, FAKE, FAKE, 10, None,
-                                 ctypes.byref(h)) == ep.EP_ERR_INVALID  # fp8 needs H % 128 == 0
+    # fresh dispatch: bad arguments rejected before planning
+    bad = [
+        (FAKE, 0, None, 100, 0, 1, FAKE, None),          # H % 8 != 0
+        (FAKE, 0, None, 256, 0, 1, FAKE + 8, None),      # misaligned output
+        (FAKE, 0, None, 200, 1, 1, FAKE, FAKE),          # fp8 needs H % 128 == 0
+        (FAKE, 1, FAKE, 256, 0, 1, FAKE, None),          # fp8 input cannot give bf16 output
+        (FAKE, 1, None, 256, 1, 1, FAKE, FAKE),          # fp8 input needs its scales
+        (FAKE, 0, FAKE, 256, 1, 1, FAKE, FAKE),          # bf16 input takes no scales
+        (FAKE, 0, None, 256, 0, 2, FAKE, None),          # column-major scales need fp8 output
+        (FAKE, 0, None, 256, 0, 8, FAKE, None),          # unknown flag
+    ]
+    for x, xd, xs, H, od, fl, rx, rs in bad:
+        assert lib.ep_dispatch_fresh(FAKE, 64, 4, 2, 8, 1, 0, x, xd, xs, H, od, fl, rx, rs, 10, None,
+                                     ctypes.byref(h)) == ep.EP_ERR_INVALID
     assert not h.value
