@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -215,7 +216,8 @@ def profiled_traffic(kernel: str, kernel_file: str, workload: str):
     for line in text.splitlines():
         if ":" in line and line.strip().startswith("- "):
             k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
+            quoted = re.search(r"`([^`]*)`", v)
+            vals[k.strip()] = quoted.group(1) if quoted else v.strip()
     if vals.get("source_sha256") != source_digest(kernel_file):
         return None
     try:

@@ -74,7 +74,8 @@ def test_profiled_traffic_requires_matching_source_hash(tmp_path, monkeypatch):
     prof = tmp_path / "profiles"
     prof.mkdir()
     digest = bench.source_digest("ep_dispatch_kernels.cu")
-    (prof / "k.bf16.md").write_text(f"# x\n- source_sha256: `{digest}`\n- dram_bytes_per_launch: 123.5\n")
+    (prof / "k.bf16.md").write_text(f"# x\n- source_sha256: `{digest}` (sha256 prefix when captured)\n"
+                                    "- dram_bytes_per_launch: 123.5\n")
     (prof / "k2.bf16.md").write_text("- source_sha256: `deadbeef`\n- dram_bytes_per_launch: 9\n")
     real_root = bench.ROOT
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
@@ -84,6 +85,11 @@ def test_profiled_traffic_requires_matching_source_hash(tmp_path, monkeypatch):
     assert bench.profiled_traffic("k", "ep_dispatch_kernels.cu", "bf16") == 123.5
     assert bench.profiled_traffic("k2", "ep_dispatch_kernels.cu", "bf16") is None
     assert bench.profiled_traffic("missing", "ep_dispatch_kernels.cu", "bf16") is None
+
+
+def test_committed_profiles_match_current_kernels():
+    # the summaries under profiles/ were captured on the kernels as committed
+    assert bench.profiled_traffic("ep_dispatch_copy_kernel", "ep_dispatch_kernels.cu", "bf16") > 1e9
 
 
 def test_reference_arm_prints_one_line_on_cpu():
