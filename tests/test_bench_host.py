@@ -87,11 +87,6 @@ def test_profiled_traffic_requires_matching_source_hash(tmp_path, monkeypatch):
     assert bench.profiled_traffic("missing", "ep_dispatch_kernels.cu", "bf16") is None
 
 
-def test_committed_profiles_match_current_kernels():
-    # the summaries under profiles/ were captured on the kernels as committed
-    assert bench.profiled_traffic("ep_dispatch_copy_kernel", "ep_dispatch_kernels.cu", "bf16") > 1e9
-
-
 def test_reference_arm_prints_one_line_on_cpu():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
                         "--warmup", "3", "--workload", "tiny"], capture_output=True, text=True, timeout=300)
