@@ -1,0 +1,67 @@
+"""GPU parity at the implementation's limits: P = EP_MAX_RANKS (1024),
+E = EP_MAX_EXPERTS (2048), K = EP_MAX_TOPK (16), and hidden sizes that leave
+partial work chunks; against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import combine_ep_plan_gb300 as ep
+import oracle
+from combine_ep_plan_gb300.inputs import WORKLOADS, bits_to_bf16_tensor, draw_hidden, draw_topk, hidden_seed
+from ep_testutil import assert_plan_equal, gpu_plan_arrays, u8, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from combine_ep_plan_gb300 import build
+    build.build()
+    ep.load_library()
+    yield
+    torch.cuda.synchronize()
+
+
+def _round_trip(w, out_dtype="bf16"):
+    idx, wts = draw_topk(w)
+    x = draw_hidden(w.T, w.H, hidden_seed(w))
+    pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
+    h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
+    assert_plan_equal(gpu_plan_arrays(h), pl)
+    xt = bits_to_bf16_tensor(x).cuda()
+    if out_dtype == "fp8":
+        q, sc = ep.dispatch(h, xt, "fp8")
+        q_ref, s_ref = oracle.dispatch_fp8(x, pl)
+        assert np.array_equal(u8(q), q_ref)
+        assert np.array_equal(sc.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    recv, _ = ep.dispatch(h, xt, "bf16")
+    ref = oracle.dispatch_bf16(x, pl)
+    assert np.array_equal(u16(recv), ref)
+    out = ep.combine(h, recv, torch.from_numpy(wts).cuda())
+    assert np.array_equal(u16(out), oracle.combine(ref, pl, wts))
+    assert h.sync_status() == ep.EP_OK
+
+
+def test_max_ranks_experts_topk():
+    # 1024 ranks x 2 experts each, 16 distinct experts per token
+    _round_trip(WORKLOADS["zipf"].scaled(P=1024, E=2048, S=4, K=16, H=256, A=8))
+
+
+def test_max_topk_uniform_wide_hidden():
+    _round_trip(WORKLOADS["bf16"].scaled(P=16, E=64, S=64, K=16, H=8192, A=16), out_dtype="fp8")
+
+
+@pytest.mark.parametrize("H", [128, 384, 2176, 16384])
+def test_fp8_partial_chunks(H):
+    # the FP8 item covers 2048 elements: H = 2176 leaves a one-group tail
+    _round_trip(WORKLOADS["fp8"].scaled(S=8, H=H), out_dtype="fp8")
+
+
+@pytest.mark.parametrize("H", [8, 24, 1032])
+def test_bf16_small_and_ragged_hidden(H):
+    # rows of 1, 3 and 129 16-byte vectors
+    _round_trip(WORKLOADS["tiny"].scaled(H=H))
+
+
+def test_one_token_per_rank():
+    _round_trip(WORKLOADS["rt"].scaled(S=1, H=256))
