@@ -183,7 +183,7 @@ ep_status_t read_status_word(ep_handle_s* h, cudaStream_t stream, bool clear, in
   }
   if (clear && st) {
     // after a timed-out wait the grid-barrier words may be off: reset them too
-    const unsigned zeros[3] = {0u, 0u, 0u};
+    const unsigned zeros[ep::kCtrWords] = {};
     e = (st & ep::kStTimeout)
             ? cudaMemcpy(h->dev.ctr, zeros, sizeof zeros, cudaMemcpyHostToDevice)
             : cudaMemcpy(h->dev.ctr + ep::kCtrStatus, zeros, sizeof(unsigned), cudaMemcpyHostToDevice);

@@ -17,11 +17,13 @@ constexpr unsigned kStDuplicate = 2u;   // same expert twice in one token row
 constexpr unsigned kStCapacity = 4u;    // an output row at or beyond capacity
 constexpr unsigned kStTimeout = 8u;     // bounded look-back wait gave up
 
-// Control words (zeroed when a handle is created).
-constexpr int kCtrBarCount = 0;  // grid barrier: CTAs arrived
-constexpr int kCtrBarGen = 1;    // grid barrier: generation
-constexpr int kCtrStatus = 2;    // device status word
-constexpr int kCtrWords = 16;
+// Control words (zeroed when a handle is created), each in its own 128-byte
+// line: the barrier's waiters poll the generation word while arrivals
+// update the count.
+constexpr int kCtrBarCount = 0;   // grid barrier: CTAs arrived
+constexpr int kCtrBarGen = 32;    // grid barrier: generation
+constexpr int kCtrStatus = 64;    // device status word
+constexpr int kCtrWords = 96;
 
 // Size slots.
 constexpr int kSizeRecv = 0;  // N_recv

@@ -5,12 +5,12 @@
 //   - a bit matrix in shared memory, one 32-bit word per (column, warp):
 //     column d < P = "token routed to rank d" (the OR deduplicates the token's
 //     slots that land on one rank), column P+e = "token picked expert e";
-//     warp-aggregated updates (__match_any_sync, one shared atomicOr per
-//     distinct key per warp); invalid and duplicate ids are reported;
+//     per-lane shared-memory atomicOr; invalid and duplicate ids are
+//     reported;
 //   - a single-pass decoupled look-back over tiles, column by column: each
 //     descriptor packs (plan epoch, state, value) in one 64-bit word, so a
 //     reader needs no fence pairs and stale descriptors of an earlier plan are
-//     ignored without clearing; eight predecessors per poll; every wait is
+//     ignored without clearing; 32 predecessors per poll; every wait is
 //     bounded;
 //   - the tile's bit matrix and its per-word exclusive prefixes go to global
 //     memory; the last tile writes the column totals.
@@ -86,30 +86,29 @@ __device__ __forceinline__ void load_tile_ids(const PlanDev& p, int64_t t0, int*
   }
 }
 
-// Builds the tile bit matrix (layout bits[w * ncols + col], zeroed before).
-// A duplicate expert in one row shows up as a bit already set when the
-// leader ORs its lane mask.
+// Builds the tile bit matrix (layout bits[w * ncols + col], zeroed before):
+// each lane ORs its own bit into the word of its expert and of the expert's
+// rank (shared-memory atomics; the OR deduplicates a token's slots on one
+// rank).  A duplicate expert in one row shows up as its bit already set.
+// (Aggregating lanes with __match_any_sync first measured slower on sm_103a
+// with ~25 distinct experts per warp.)
 __device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids, uint32_t* bits) {
-  const int lane = threadIdx.x & 31;
-  const int w = threadIdx.x >> 5;
+  const unsigned me = 1u << (threadIdx.x & 31);
+  uint32_t* row = bits + (threadIdx.x >> 5) * p.ncols;
   for (int k = 0; k < p.K; ++k) {
     const int e = ids[threadIdx.x * p.K + k];
-    const unsigned me = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(me) - 1) {
-      unsigned old = atomicOr(&bits[w * p.ncols + p.P + e], me);
-      if (old & me) atomicOr(&p.ctr[kCtrStatus], kStDuplicate);
-    }
-    const int d = e >= 0 ? e / p.El : -1;
-    const unsigned md = __match_any_sync(0xffffffffu, d);
-    if (d >= 0 && lane == __ffs(md) - 1) atomicOr(&bits[w * p.ncols + d], md);
+    if (e < 0) continue;
+    const unsigned old = atomicOr(&row[p.P + e], me);
+    if (old & me) atomicOr(&p.ctr[kCtrStatus], kStDuplicate);
+    atomicOr(&row[e / p.El], me);
   }
 }
 
 // Exclusive prefix of one column over all earlier tiles: walk back through
-// predecessors sixteen at a time, adding aggregates until an inclusive prefix
+// predecessors 32 at a time, adding aggregates until an inclusive prefix
 // is found.  A descriptor of another epoch counts as not yet published.
 __device__ int lookback(const PlanDev& p, int tile, int col, bool* timed_out) {
-  constexpr int kWindow = 16;
+  constexpr int kWindow = 32;
   int sum = 0;
   int j = tile - 1;
   long long polls = 0;
@@ -184,50 +183,97 @@ __device__ __forceinline__ int x_at(const PlanDev& p, int col, int64_t g) {
   return __ldcg(&p.tile_wpre[at]) + __popc(__ldcg(&p.tile_bits[at]) & lanes_below(gl & 31));
 }
 
-// Exclusive scan of n ints in shared memory by one CTA of kTile threads
-// (each thread a contiguous run, warp shuffles across threads); returns the
-// total.  `warp_sums` holds kTile/32 ints.
-__device__ int block_exclusive_scan(int* a, int n, int* warp_sums) {
+// One warp turns the column totals into the offsets, in shared memory:
+// expert segments padded to A (exp_off), padding rows per expert (pad_off)
+// and receive windows (recv_off), each an exclusive scan with its total at
+// the end; sizes[] gets {N_recv, N_exp, N_pad}.  Each lane scans a
+// contiguous run of each array, one shuffle scan joins the lanes.
+__device__ void offsets_warp_scan(const PlanDev& p, int* exp_off, int* pad_off, int* recv_off, int* sizes) {
   const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int per = (n + kTile - 1) / kTile;
-  const int lo = threadIdx.x * per;
-  int sum = 0;
-  for (int i = 0; i < per; ++i)
-    if (lo + i < n) sum += a[lo + i];
-  int incl = sum;
+  const int per_e = (p.E + 31) / 32;
+  const int per_d = (p.P + 31) / 32;
+  const int lo_e = lane * per_e;
+  const int lo_d = lane * per_d;
+  int sum_exp = 0, sum_pad = 0, sum_recv = 0;
+  constexpr int kBatch = 8;  // loads issued before any is used
+  for (int i0 = 0; i0 < per_e; i0 += kBatch) {
+    int n[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int e = lo_e + i0 + u;
+      n[u] = (i0 + u < per_e && e < p.E) ? __ldcg(&p.totals[p.P + e]) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int e = lo_e + i0 + u;
+      if (i0 + u < per_e && e < p.E) {
+        const int v = (n[u] + p.A - 1) / p.A * p.A;
+        exp_off[e] = v;
+        pad_off[e] = v - n[u];
+        sum_exp += v;
+        sum_pad += v - n[u];
+      }
+    }
+  }
+  for (int i0 = 0; i0 < per_d; i0 += kBatch) {
+    int n[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int d = lo_d + i0 + u;
+      n[u] = (i0 + u < per_d && d < p.P) ? __ldcg(&p.totals[d]) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int d = lo_d + i0 + u;
+      if (i0 + u < per_d && d < p.P) {
+        recv_off[d] = n[u];
+        sum_recv += n[u];
+      }
+    }
+  }
+  int inc_exp = sum_exp, inc_pad = sum_pad, inc_recv = sum_recv;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, incl, off);
-    if (lane >= off) incl += v;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kTile / 32 ? warp_sums[lane] : 0;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, w, off);
-      if (lane >= off) w += v;
+    const int a = __shfl_up_sync(0xffffffffu, inc_exp, off);
+    const int b = __shfl_up_sync(0xffffffffu, inc_pad, off);
+    const int c = __shfl_up_sync(0xffffffffu, inc_recv, off);
+    if (lane >= off) {
+      inc_exp += a;
+      inc_pad += b;
+      inc_recv += c;
     }
-    if (lane < kTile / 32) warp_sums[lane] = w;  // inclusive over warps
   }
-  __syncthreads();
-  int run = incl - sum + (warp > 0 ? warp_sums[warp - 1] : 0);
-  for (int i = 0; i < per; ++i)
-    if (lo + i < n) {
-      const int v = a[lo + i];
-      a[lo + i] = run;
-      run += v;
+  int run_exp = inc_exp - sum_exp, run_pad = inc_pad - sum_pad, run_recv = inc_recv - sum_recv;
+  for (int i = 0; i < per_e; ++i) {
+    const int e = lo_e + i;
+    if (e < p.E) {
+      const int ve = exp_off[e], vp = pad_off[e];
+      exp_off[e] = run_exp;
+      pad_off[e] = run_pad;
+      run_exp += ve;
+      run_pad += vp;
     }
-  const int total = warp_sums[kTile / 32 - 1];
-  __syncthreads();
-  return total;
+  }
+  for (int i = 0; i < per_d; ++i) {
+    const int d = lo_d + i;
+    if (d < p.P) {
+      const int v = recv_off[d];
+      recv_off[d] = run_recv;
+      run_recv += v;
+    }
+  }
+  if (lane == 31) {
+    exp_off[p.E] = inc_exp;
+    pad_off[p.E] = inc_pad;
+    recv_off[p.P] = inc_recv;
+    sizes[kSizeRecv] = inc_recv;
+    sizes[kSizeExp] = inc_exp;
+    sizes[kSizePad] = inc_pad;
+  }
 }
 
 __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   extern __shared__ __align__(16) uint32_t smem[];
-  __shared__ int scan_scratch[3][kTile / 32];
 
   // ---------------- phase 1: tiles ----------------
   uint32_t* bits = smem;                                           // [kTileWords * ncols]
@@ -277,23 +323,12 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   int* exp_off = reinterpret_cast<int*>(smem);  // [E+1]
   int* pad_off = exp_off + (p.E + 1);           // [E+1]
   int* recv_off = pad_off + (p.E + 1);          // [P+1]
-  for (int e = threadIdx.x; e < p.E; e += blockDim.x) {
-    const int n = __ldcg(&p.totals[p.P + e]);
-    const int v = (n + p.A - 1) / p.A * p.A;
-    exp_off[e] = v;
-    pad_off[e] = v - n;
-  }
-  for (int d = threadIdx.x; d < p.P; d += blockDim.x) recv_off[d] = __ldcg(&p.totals[d]);
+  __shared__ int s_sizes[3];
+  if (threadIdx.x < 32) offsets_warp_scan(p, exp_off, pad_off, recv_off, s_sizes);
   __syncthreads();
-  const int n_exp = block_exclusive_scan(exp_off, p.E, scan_scratch[0]);
-  const int n_pad = block_exclusive_scan(pad_off, p.E, scan_scratch[1]);
-  const int n_recv = block_exclusive_scan(recv_off, p.P, scan_scratch[2]);
-  if (threadIdx.x == 0) {
-    exp_off[p.E] = n_exp;
-    pad_off[p.E] = n_pad;
-    recv_off[p.P] = n_recv;
-  }
-  __syncthreads();
+  const int n_recv = s_sizes[kSizeRecv];
+  const int n_exp = s_sizes[kSizeExp];
+  const int n_pad = s_sizes[kSizePad];
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
       p.exp_off[i] = exp_off[i];
@@ -310,14 +345,36 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
 
-  // slot and exp_src, one token per thread
+  // slot and exp_src, one token per thread: the token's K ids, then all
+  // their window positions, are loaded before any is used.
   for (int64_t g = gtid; g < p.T; g += nthr) {
-    for (int k = 0; k < p.K; ++k) {
-      const long long v = p.topk_idx[g * p.K + k];
+    int e[EP_MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < EP_MAX_TOPK; ++k) {
+      const long long v = k < p.K ? p.topk_idx[g * p.K + k] : -1ll;
+      e[k] = (v >= 0 && v < p.E) ? static_cast<int>(v) : -1;
+    }
+    const int64_t t = g / kTile;
+    const int gl = static_cast<int>(g - t * kTile);
+    const int64_t word = (t * kTileWords + (gl >> 5)) * p.ncols + p.P;
+    int pre[EP_MAX_TOPK];
+    uint32_t bw[EP_MAX_TOPK];
+#pragma unroll
+    for (int k = 0; k < EP_MAX_TOPK; ++k) {
+      pre[k] = 0;
+      bw[k] = 0u;
+      if (e[k] >= 0) {
+        pre[k] = __ldcg(&p.tile_wpre[word + e[k]]);
+        bw[k] = __ldcg(&p.tile_bits[word + e[k]]);
+      }
+    }
+    const uint32_t below = lanes_below(gl & 31);
+#pragma unroll
+    for (int k = 0; k < EP_MAX_TOPK; ++k) {
+      if (k >= p.K) break;
       int r = -1;
-      if (v >= 0 && v < p.E) {
-        const int e = static_cast<int>(v);
-        r = exp_off[e] + x_at(p, p.P + e, g);
+      if (e[k] >= 0) {
+        r = exp_off[e[k]] + pre[k] + __popc(bw[k] & below);
         p.exp_src[r] = static_cast<int>(g);
       }
       p.slot[g * p.K + k] = r;
@@ -364,7 +421,9 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
 
   // prefix matrices, one (s, d, c) per thread; layout of i is [s][d][c]
 #pragma unroll 2
-  for (int64_t i = gtid; i < static_cast<int64_t>(p.P) * p.P * p.C; i += nthr) {
+  // The small passes below start at different points of the thread range,
+  // so that they do not all land on the first CTAs after the slot pass.
+  for (int64_t i = (gtid + nthr / 2) % nthr; i < static_cast<int64_t>(p.P) * p.P * p.C; i += nthr) {
     const int c = static_cast<int>(i % p.C);
     const int64_t sd = i / p.C;
     const int d = static_cast<int>(sd % p.P);
@@ -383,14 +442,14 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   }
 
   // per-source expert counts
-  for (int i = static_cast<int>(gtid); i < p.P * p.E; i += static_cast<int>(nthr)) {
+  for (int i = static_cast<int>((gtid + 3 * nthr / 4) % nthr); i < p.P * p.E; i += static_cast<int>(nthr)) {
     const int s = i / p.E;
     const int e = i - s * p.E;
     p.ntpe[i] = x_at(p, p.P + e, (s + 1) * p.S) - x_at(p, p.P + e, static_cast<int64_t>(s) * p.S);
   }
 
   // padding rows of the expanded layout
-  for (int64_t i = gtid; i < n_pad; i += nthr) {
+  for (int64_t i = (gtid + nthr / 4) % nthr; i < n_pad; i += nthr) {
     int lo = 0, hi = p.E;  // e with pad_off[e] <= i < pad_off[e+1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
