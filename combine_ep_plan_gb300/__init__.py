@@ -22,6 +22,7 @@ __all__ = [
     "EPError", "EPHandle", "plan", "dispatch", "dispatch_fresh", "dispatch_cached", "combine",
     "worst_expanded_rows", "library_path", "load_library", "FIELDS", "set_lookback_debug",
     "dispatch_backward", "combine_backward", "dispatch_metadata",
+    "Pending", "dispatch_async", "combine_async", "PROFILE_KERNELS", "PROFILE_WORDS", "summarize_profile",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -117,6 +118,19 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ep_handle_destroy.argtypes = [vp, vp]
     lib.ep_debug_set_lookback.restype = None
     lib.ep_debug_set_lookback.argtypes = [i64, i32]
+    lib.ep_set_num_sms.restype = st
+    lib.ep_set_num_sms.argtypes = [vp, i32]
+    lib.ep_dispatch_async.restype = st
+    lib.ep_dispatch_async.argtypes = [vp, vp, vp, i32, vp, i64, i32, i32, vp, vp, i64, vp, vp, i32,
+                                      ctypes.POINTER(vp)]
+    lib.ep_combine_async.restype = st
+    lib.ep_combine_async.argtypes = [vp, vp, i64, vp, vp, i64, vp, vp, vp, i32, ctypes.POINTER(vp)]
+    lib.ep_pending_wait.restype = st
+    lib.ep_pending_wait.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    lib.ep_profile_begin.restype = st
+    lib.ep_profile_begin.argtypes = [vp, vp, i64]
+    lib.ep_profile_end.restype = st
+    lib.ep_profile_end.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i64)]
     _LIB = lib
     return lib
 
@@ -211,9 +225,28 @@ class EPHandle:
     def check(self, stream: Optional[torch.cuda.Stream] = None):
         _check(self.sync_status(stream), "device status")
 
+    def set_num_sms(self, num_sms: int):
+        """SM budget of this handle's kernels (0 = the whole device)."""
+        _check(_lib().ep_set_num_sms(self.ptr, int(num_sms)), "ep_set_num_sms")
+
+    def profile_begin(self, capacity: int = 1 << 16):
+        """Start per-CTA profile records (capacity records of PROFILE_WORDS uint64)."""
+        self._prof = torch.zeros((capacity, PROFILE_WORDS), dtype=torch.int64, device=f"cuda:{self.device}")
+        _check(_lib().ep_profile_begin(self.ptr, self._prof.data_ptr(), capacity), "ep_profile_begin")
+
+    def profile_end(self, stream: Optional[torch.cuda.Stream] = None):
+        """Stop recording; synchronise `stream` and return (records [n, 8]
+        int64 on the host, dropped count)."""
+        n, dropped = ctypes.c_int64(), ctypes.c_int64()
+        _check(_lib().ep_profile_end(self.ptr, ctypes.byref(n), ctypes.byref(dropped)), "ep_profile_end")
+        (stream or torch.cuda.current_stream()).synchronize()
+        rec = self._prof[: n.value].cpu()
+        self._prof = None
+        return rec, dropped.value
+
     def destroy(self, stream: Optional[torch.cuda.Stream] = None):
         if self._ptr:
-            _lib().ep_handle_destroy(self._ptr, _stream_ptr(stream))
+            _check(_lib().ep_handle_destroy(self._ptr, _stream_ptr(stream)), "ep_handle_destroy")
             self._ptr = 0
 
     def __del__(self):
@@ -462,6 +495,149 @@ def combine_backward(handle: EPHandle, grad_out: torch.Tensor, y: torch.Tensor, 
                                       grad_y.shape[0], grad_weights.data_ptr(), _stream_ptr(stream)),
            "ep_combine_backward")
     return grad_y, grad_weights
+
+
+class Pending:
+    """An issued dispatch_async / combine_async.  wait() must be called once:
+    it makes the compute stream wait for the issued work (no host block) and
+    returns the results.  The pending object keeps the tensors the work uses
+    alive until then."""
+
+    def __init__(self, ptr: int, kind: str, results, keep):
+        self._ptr = ptr
+        self.kind = kind
+        self._results = results
+        self._keep = keep
+
+    def wait(self):
+        """dispatch: (recv_x, recv_scales|None, N_exp, N_recv); combine: out."""
+        if not self._ptr:
+            raise RuntimeError("pending call already waited on")
+        ne, nr = ctypes.c_int64(), ctypes.c_int64()
+        want = self.kind == "dispatch"
+        code = _lib().ep_pending_wait(self._ptr, ctypes.byref(ne) if want else None,
+                                      ctypes.byref(nr) if want else None)
+        self._ptr = 0
+        self._keep = None
+        _check(code, "ep_pending_wait")
+        if want:
+            return self._results[0], self._results[1], ne.value, nr.value
+        return self._results
+
+    def __del__(self):
+        try:
+            if self._ptr and _LIB is not None:
+                _LIB.ep_pending_wait(self._ptr, None, None)
+        except Exception:
+            pass
+
+
+def _event_ptr(previous) -> Optional[int]:
+    if previous is None:
+        return None
+    ptr = int(previous.cuda_event)
+    if not ptr:
+        raise ValueError("previous event has never been recorded")
+    return ptr
+
+
+def dispatch_async(handle: EPHandle, x: torch.Tensor, out_dtype: str = "bf16", zero_pad: bool = True,
+                   recv_x: Optional[torch.Tensor] = None, recv_scales: Optional[torch.Tensor] = None,
+                   topk_idx: Optional[torch.Tensor] = None, previous: Optional[torch.cuda.Event] = None,
+                   defer_epilogue: bool = True, stream: Optional[torch.cuda.Stream] = None,
+                   x_scales: Optional[torch.Tensor] = None, scales_col_major: bool = False) -> Pending:
+    """Issue a dispatch on the handle's communication stream and return at
+    once (defer_epilogue=True) or once the plan's counts are known
+    (defer_epilogue=False).  topk_idx re-plans first (fresh dispatch); None
+    uses the handle's plan (cached dispatch).  Outputs default to the
+    worst-case row count.  `stream` is the compute stream the work is ordered
+    after (unless `previous` is given) and that wait() joins."""
+    code = _dtype_code(out_dtype)
+    xcode = _input_code(x, x_scales)
+    H = x.shape[1]
+    if topk_idx is not None:
+        _need(topk_idx, "topk_idx", torch.int64, 2)
+        if tuple(topk_idx.shape) != (handle.T, handle.K):
+            raise ValueError("topk_idx must be [T,K] of the handle")
+        handle._sizes = None
+    cap = worst_expanded_rows(handle.T, handle.K, handle.E, handle.A)
+    recv_x, recv_scales = _dispatch_outputs(H, out_dtype, recv_x, recv_scales, cap, x.device, scales_col_major)
+    _check_dispatch(x, recv_x, recv_scales, out_dtype, scales_col_major)
+    p = ctypes.c_void_p()
+    _check(_lib().ep_dispatch_async(handle.ptr, topk_idx.data_ptr() if topk_idx is not None else None,
+                                    x.data_ptr(), xcode, x_scales.data_ptr() if x_scales is not None else None,
+                                    H, code, _flags(zero_pad, scales_col_major), recv_x.data_ptr(),
+                                    recv_scales.data_ptr() if recv_scales is not None else None,
+                                    recv_x.shape[0], _stream_ptr(stream), _event_ptr(previous),
+                                    int(bool(defer_epilogue)), ctypes.byref(p)), "ep_dispatch_async")
+    return Pending(p.value, "dispatch", (recv_x, recv_scales), (x, x_scales, topk_idx, previous))
+
+
+def combine_async(handle: EPHandle, y: torch.Tensor, topk_weights: torch.Tensor,
+                  out: Optional[torch.Tensor] = None, bias: Optional[torch.Tensor] = None,
+                  previous: Optional[torch.cuda.Event] = None, defer_epilogue: bool = True,
+                  stream: Optional[torch.cuda.Stream] = None) -> Pending:
+    """Issue a combine on the handle's communication stream; wait() -> out."""
+    _need(y, "y", torch.bfloat16, 2)
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, 2)
+        if tuple(bias.shape) != (handle.T, y.shape[1]):
+            raise ValueError("bias must be [T,H]")
+    _need(topk_weights, "topk_weights", torch.float32, 2)
+    if tuple(topk_weights.shape) != (handle.T, handle.K):
+        raise ValueError("topk_weights must be [T,K]")
+    H = y.shape[1]
+    if out is None:
+        out = torch.empty((handle.T, H), dtype=torch.bfloat16, device=y.device)
+    _need(out, "out", torch.bfloat16, 2)
+    if tuple(out.shape) != (handle.T, H):
+        raise ValueError("out must be [T,H]")
+    p = ctypes.c_void_p()
+    _check(_lib().ep_combine_async(handle.ptr, y.data_ptr(), y.shape[0], topk_weights.data_ptr(),
+                                   bias.data_ptr() if bias is not None else None, H, out.data_ptr(),
+                                   _stream_ptr(stream), _event_ptr(previous), int(bool(defer_epilogue)),
+                                   ctypes.byref(p)), "ep_combine_async")
+    return Pending(p.value, "combine", out, (y, topk_weights, bias, previous))
+
+
+# Per-CTA profile records (ep_profile_begin): kernel ids and record width.
+PROFILE_KERNELS = {1: "plan", 2: "dispatch_bf16", 3: "dispatch_fp8", 4: "dispatch_fp8_input", 5: "combine",
+                   6: "dispatch_backward"}
+PROFILE_WORDS = 8
+
+
+def summarize_profile(records) -> list:
+    """Aggregate per-CTA records (an [n, 8] int64 array or tensor) per launch,
+    in launch order: kernel, CTAs, units, payload bytes, span from the first
+    CTA start to the last CTA end (ns), median and max CTA duration (ns),
+    payload GB/s over the span, and for the plan the median stage offsets
+    from the launch's first start (route scan, phase 1, barrier), in ns."""
+    import numpy as np
+    r = np.asarray(records.cpu() if isinstance(records, torch.Tensor) else records).astype(np.uint64)
+    if r.size == 0:
+        return []
+    r = r.reshape(-1, PROFILE_WORDS)
+    kind = (r[:, 0] >> np.uint64(56)).astype(np.int64)
+    seq = ((r[:, 0] >> np.uint64(32)) & np.uint64(0xFFFFFF)).astype(np.int64)
+    out = []
+    for s in sorted(set(seq.tolist()), key=lambda v: int(np.argmax(seq == v))):
+        m = seq == s
+        k = int(kind[m][0])
+        t0, t1 = r[m, 1].astype(np.int64), r[m, 5].astype(np.int64)
+        span = int(t1.max() - t0.min())
+        nbytes = int(r[m, 7].sum())
+        row = {"seq": int(s), "kernel": PROFILE_KERNELS.get(k, str(k)), "ctas": int(m.sum()),
+               "units": int(r[m, 6].sum()), "bytes": nbytes, "span_ns": span,
+               "cta_ns_median": float(np.median(t1 - t0)), "cta_ns_max": int((t1 - t0).max()),
+               "gbs": nbytes / span if span > 0 else 0.0}
+        if k == 1:
+            base = t0.min()
+            for name, col in (("scan_ns", 2), ("phase1_ns", 3), ("barrier_ns", 4)):
+                v = r[m, col].astype(np.int64)
+                v = v[v > 0]
+                row[name] = float(np.median(v - base)) if len(v) else 0.0
+        out.append(row)
+    return out
 
 
 def set_lookback_debug(poll_limit: int = 0, suppress_tile: int = -1):

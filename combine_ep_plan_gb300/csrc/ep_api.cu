@@ -19,7 +19,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 2;
+constexpr int kAbiVersion = 3;
 constexpr long long kDefaultPollLimit = 1ll << 20;
 
 long long g_poll_limit = kDefaultPollLimit;
@@ -37,6 +37,10 @@ struct Layout {
 
 }  // namespace
 
+// Pinned host slots for the counts an asynchronous dispatch reads back.
+constexpr int kCountSlots = 8;
+constexpr int kCountWords = 4;  // N_recv, N_exp, N_pad, status word
+
 struct ep_handle_s {
   ep::PlanDev dev;
   void* base = nullptr;
@@ -45,6 +49,28 @@ struct ep_handle_s {
   int64_t cap_recv = 0, cap_exp = 0, cap_pad = 0;
   int device = 0;
   unsigned epoch = 0;
+  // SM budget of the dispatch, combine and backward launches (0 = all)
+  int sm_budget = 0;
+  // asynchronous calls: communication stream, pinned count slots in use,
+  // pending objects not yet waited on
+  cudaStream_t comm = nullptr;
+  unsigned* counts_host = nullptr;  // [kCountSlots][kCountWords], pinned
+  unsigned slots_used = 0;
+  int outstanding = 0;
+  // per-CTA profile records
+  unsigned long long* prof_rec = nullptr;
+  long long prof_cap = 0, prof_next = 0;
+  unsigned prof_seq = 0;
+};
+
+struct ep_pending_s {
+  ep_handle_s* h = nullptr;
+  cudaStream_t compute = nullptr;
+  cudaEvent_t counted = nullptr;  // dispatch: the counts are in the pinned slot
+  cudaEvent_t done = nullptr;     // all issued work
+  int slot = -1;                  // pinned count slot (dispatch), else -1
+  bool have_counts = false;
+  unsigned counts[kCountWords] = {0, 0, 0, 0};
 };
 
 namespace ep {
@@ -86,6 +112,38 @@ void keep_pool_memory(int dev) {
       cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
     }
   });
+}
+
+// The launch shape for a handle's kernel: its SM budget, and the next
+// profile records when profiling is on.  finish_launch advances the record
+// cursor by the CTAs the launch used.
+struct Launch {
+  ep::LaunchCfg cfg;
+  long long ctas = 0;
+  unsigned long long* prof_rec = nullptr;
+  long long prof_meta = 0;
+  explicit Launch(const ep_handle_s* h) {
+    cfg.sm_budget = h->sm_budget;
+    cfg.ctas = &ctas;
+    if (h->prof_rec) {
+      const long long at = h->prof_next < h->prof_cap ? h->prof_next : h->prof_cap;
+      prof_rec = h->prof_rec + at * ep::kProfWords;
+      prof_meta = (static_cast<long long>(h->prof_seq & 0xffffffu) << ep::kProfAvailBits) | (h->prof_cap - at);
+    }
+  }
+  template <class Dev>
+  void target(Dev& d) const {
+    d.prof_rec = prof_rec;
+    d.prof_meta = prof_meta;
+  }
+};
+
+cudaError_t finish_launch(ep_handle_s* h, const Launch& L, cudaError_t e) {
+  if (e == cudaSuccess && h->prof_rec) {
+    h->prof_next += L.ctas;
+    h->prof_seq = (h->prof_seq + 1u) & 0xffffffu;
+  }
+  return e;
 }
 
 ep_status_t check_shape(int64_t S, int P, int K, int E, int A, int* C) {
@@ -168,7 +226,9 @@ ep_status_t enqueue_plan(ep_handle_s* h, const int64_t* topk_idx, cudaStream_t s
   h->epoch = (h->epoch + 1u) & 0x3fffffffu;
   if (h->epoch == 0u) h->epoch = 1u;  // epoch 0 is what cleared memory holds
   h->dev.epoch = h->epoch;
-  return cuda_status(ep::launch_plan(h->dev, stream));
+  Launch L(h);
+  L.target(h->dev);
+  return cuda_status(finish_launch(h, L, ep::launch_plan(h->dev, stream, L.cfg)));
 }
 
 ep_status_t read_status_word(ep_handle_s* h, cudaStream_t stream, bool clear, int sizes[3]) {
@@ -325,14 +385,16 @@ ep_status_t ep_dispatch(ep_handle_t h, const void* x, ep_dtype_t x_dtype, const 
   d.max_pad = zero_pad ? h->cap_pad : 0;
   d.zero_pad = zero_pad ? 1 : 0;
   d.scales_col_major = (flags & EP_DISPATCH_SCALES_COL_MAJOR) ? 1 : 0;
+  Launch L(h);
+  L.target(d);
   cudaError_t e;
   if (x_dtype == EP_DTYPE_FP8_E4M3)
-    e = ep::launch_dispatch_fp8_input(d, stream);
+    e = ep::launch_dispatch_fp8_input(d, stream, L.cfg);
   else if (out_dtype == EP_DTYPE_BF16)
-    e = ep::launch_dispatch_bf16(d, stream);
+    e = ep::launch_dispatch_bf16(d, stream, L.cfg);
   else
-    e = ep::launch_dispatch_fp8(d, stream);
-  return cuda_status(e);
+    e = ep::launch_dispatch_fp8(d, stream, L.cfg);
+  return cuda_status(finish_launch(h, L, e));
 }
 
 ep_status_t ep_dispatch_cached(ep_handle_t h, int E, int A, int64_t S, const void* x, ep_dtype_t x_dtype,
@@ -402,7 +464,9 @@ ep_status_t ep_combine(ep_handle_t h, const void* y, int64_t y_rows, const float
   c.K = h->dev.K;
   c.H = H;
   c.y_rows = y_rows;
-  return cuda_status(ep::launch_combine(c, reinterpret_cast<cudaStream_t>(stream)));
+  Launch L(h);
+  L.target(c);
+  return cuda_status(finish_launch(h, L, ep::launch_combine(c, reinterpret_cast<cudaStream_t>(stream), L.cfg)));
 }
 
 ep_status_t ep_dispatch_backward(ep_handle_t h, const void* grad_recv, int64_t grad_rows, int64_t H,
@@ -420,7 +484,9 @@ ep_status_t ep_dispatch_backward(ep_handle_t h, const void* grad_recv, int64_t g
   c.K = h->dev.K;
   c.H = H;
   c.y_rows = grad_rows;
-  return cuda_status(ep::launch_combine(c, reinterpret_cast<cudaStream_t>(stream)));
+  Launch L(h);
+  L.target(c);
+  return cuda_status(finish_launch(h, L, ep::launch_combine(c, reinterpret_cast<cudaStream_t>(stream), L.cfg)));
 }
 
 ep_status_t ep_combine_backward(ep_handle_t h, const void* grad_out, const void* y, int64_t y_rows,
@@ -448,7 +514,8 @@ ep_status_t ep_combine_backward(ep_handle_t h, const void* grad_out, const void*
   c.y_rows = y_rows;
   c.grad_y_rows = grad_y_rows;
   c.max_pad = zero_pad ? h->cap_pad : 0;
-  return cuda_status(ep::launch_combine_backward(c, reinterpret_cast<cudaStream_t>(stream)));
+  Launch L(h);  // not profiled: the combine backward has no record variant
+  return cuda_status(ep::launch_combine_backward(c, reinterpret_cast<cudaStream_t>(stream), L.cfg));
 }
 
 ep_status_t ep_sync_status(ep_handle_t h, ep_stream_t stream) {
@@ -493,12 +560,230 @@ ep_status_t ep_handle_info(ep_handle_t h, int64_t* S, int* P, int* K, int* E, in
   return EP_OK;
 }
 
-ep_status_t ep_handle_destroy(ep_handle_t h, ep_stream_t stream) {
+ep_status_t ep_handle_destroy(ep_handle_t h, ep_stream_t stream_) {
   if (!h) return EP_ERR_INVALID;
+  if (h->outstanding > 0) return EP_ERR_INVALID;  // wait on its pending calls first
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   cudaError_t e = cudaSuccess;
-  if (h->base) e = cudaFreeAsync(h->base, reinterpret_cast<cudaStream_t>(stream));
+  if (h->comm) {
+    // the communication stream's work ends before the memory is released
+    e = cudaStreamSynchronize(h->comm);
+    cudaStreamDestroy(h->comm);
+    if (h->counts_host) cudaFreeHost(h->counts_host);
+  }
+  if (h->base) {
+    const cudaError_t e2 = cudaFreeAsync(h->base, stream);
+    if (e == cudaSuccess) e = e2;
+  }
   delete h;
   return cuda_status(e);
+}
+
+ep_status_t ep_set_num_sms(ep_handle_t h, int num_sms) {
+  if (!h || num_sms < 0) return EP_ERR_INVALID;
+  h->sm_budget = num_sms >= ep::num_sms() ? 0 : num_sms;
+  return EP_OK;
+}
+
+ep_status_t ep_profile_begin(ep_handle_t h, uint64_t* records, int64_t capacity) {
+  if (!h || !records || capacity < 1 || capacity >= (1ll << ep::kProfAvailBits) || !aligned(records, 8))
+    return EP_ERR_INVALID;
+  h->prof_rec = reinterpret_cast<unsigned long long*>(records);
+  h->prof_cap = capacity;
+  h->prof_next = 0;
+  h->prof_seq = 0;
+  return EP_OK;
+}
+
+ep_status_t ep_profile_end(ep_handle_t h, int64_t* written, int64_t* dropped) {
+  if (!h || !h->prof_rec) return EP_ERR_INVALID;
+  const long long n = h->prof_next;
+  if (written) *written = n < h->prof_cap ? n : h->prof_cap;
+  if (dropped) *dropped = n > h->prof_cap ? n - h->prof_cap : 0;
+  h->prof_rec = nullptr;
+  h->prof_cap = h->prof_next = 0;
+  return EP_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+// The communication stream and the pinned count slots, made on first use.
+ep_status_t ensure_comm(ep_handle_s* h) {
+  if (h->comm) return EP_OK;
+  int cur = 0;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (cur != h->device) return EP_ERR_INVALID;
+  e = cudaHostAlloc(reinterpret_cast<void**>(&h->counts_host), sizeof(unsigned) * kCountSlots * kCountWords,
+                    cudaHostAllocDefault);
+  if (e != cudaSuccess) return cuda_status(e);
+  std::memset(h->counts_host, 0, sizeof(unsigned) * kCountSlots * kCountWords);
+  e = cudaStreamCreateWithFlags(&h->comm, cudaStreamNonBlocking);
+  if (e != cudaSuccess) {
+    cudaFreeHost(h->counts_host);
+    h->counts_host = nullptr;
+    h->comm = nullptr;
+    return cuda_status(e);
+  }
+  return EP_OK;
+}
+
+// A pending object with its events; the communication stream is ordered
+// after `previous`, or after everything enqueued on `compute` so far.
+ep_status_t begin_async(ep_handle_s* h, cudaStream_t compute, cudaEvent_t previous, bool counts,
+                        ep_pending_s** out) {
+  ep_status_t st = ensure_comm(h);
+  if (st != EP_OK) return st;
+  int slot = -1;
+  if (counts) {
+    for (int i = 0; i < kCountSlots; ++i)
+      if (!(h->slots_used & (1u << i))) {
+        slot = i;
+        break;
+      }
+    if (slot < 0) return EP_ERR_CAPACITY;  // too many dispatches in flight
+  }
+  ep_pending_s* p = new (std::nothrow) ep_pending_s();
+  if (!p) return EP_ERR_OOM;
+  p->h = h;
+  p->compute = compute;
+  p->slot = slot;
+  cudaError_t e = cudaEventCreateWithFlags(&p->done, cudaEventDisableTiming);
+  if (e == cudaSuccess && counts) e = cudaEventCreateWithFlags(&p->counted, cudaEventDisableTiming);
+  cudaEvent_t ready = previous;
+  if (e == cudaSuccess && !ready) {
+    e = cudaEventCreateWithFlags(&ready, cudaEventDisableTiming);
+    if (e == cudaSuccess) {
+      e = cudaEventRecord(ready, compute);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(h->comm, ready, 0);
+      cudaEventDestroy(ready);  // released once the wait no longer needs it
+    }
+  } else if (e == cudaSuccess) {
+    e = cudaStreamWaitEvent(h->comm, ready, 0);
+  }
+  if (e != cudaSuccess) {
+    if (p->done) cudaEventDestroy(p->done);
+    if (p->counted) cudaEventDestroy(p->counted);
+    delete p;
+    return cuda_status(e);
+  }
+  if (slot >= 0) h->slots_used |= 1u << slot;
+  ++h->outstanding;
+  *out = p;
+  return EP_OK;
+}
+
+// Copies the sizes and the status word to the pending object's pinned slot,
+// on the communication stream, and marks it.
+cudaError_t enqueue_counts(ep_pending_s* p) {
+  ep_handle_s* h = p->h;
+  unsigned* dst = h->counts_host + p->slot * kCountWords;
+  cudaError_t e = cudaMemcpyAsync(dst, h->dev.sizes, sizeof(unsigned) * 3, cudaMemcpyDeviceToHost, h->comm);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(dst + 3, h->dev.ctr + ep::kCtrStatus, sizeof(unsigned), cudaMemcpyDeviceToHost, h->comm);
+  if (e == cudaSuccess) e = cudaEventRecord(p->counted, h->comm);
+  return e;
+}
+
+// The host side of the epilogue: wait for the counts, keep them.
+ep_status_t read_counts(ep_pending_s* p) {
+  if (p->have_counts || p->slot < 0) return EP_OK;
+  cudaError_t e = cudaEventSynchronize(p->counted);
+  if (e != cudaSuccess) return cuda_status(e);
+  std::memcpy(p->counts, p->h->counts_host + p->slot * kCountWords, sizeof p->counts);
+  p->have_counts = true;
+  return EP_OK;
+}
+
+ep_status_t status_of(unsigned st) {
+  if (st & (ep::kStInvalidId | ep::kStDuplicate)) return EP_ERR_INVALID;
+  if (st & ep::kStTimeout) return EP_ERR_TIMEOUT;
+  if (st & ep::kStCapacity) return EP_ERR_CAPACITY;
+  return EP_OK;
+}
+
+void release_pending(ep_pending_s* p) {
+  ep_handle_s* h = p->h;
+  if (p->slot >= 0) h->slots_used &= ~(1u << p->slot);
+  --h->outstanding;
+  if (p->counted) cudaEventDestroy(p->counted);
+  if (p->done) cudaEventDestroy(p->done);
+  delete p;
+}
+
+}  // namespace
+
+extern "C" {
+
+ep_status_t ep_dispatch_async(ep_handle_t h, const int64_t* topk_idx, const void* x, ep_dtype_t x_dtype,
+                              const float* x_scales, int64_t H, ep_dtype_t out_dtype, int flags, void* recv_x,
+                              float* recv_scales, int64_t capacity, ep_stream_t compute_, ep_event_t previous,
+                              int defer_epilogue, ep_pending_t* out) {
+  if (!out) return EP_ERR_INVALID;
+  *out = nullptr;
+  ep_status_t st = check_dispatch_args(h, x, x_dtype, x_scales, H, out_dtype, flags, recv_x, recv_scales, capacity);
+  if (st != EP_OK) return st;
+  if (topk_idx && !aligned(topk_idx, 8)) return EP_ERR_INVALID;
+  ep_pending_s* p = nullptr;
+  st = begin_async(h, reinterpret_cast<cudaStream_t>(compute_), reinterpret_cast<cudaEvent_t>(previous), true, &p);
+  if (st != EP_OK) return st;
+  ep_stream_t comm = reinterpret_cast<ep_stream_t>(h->comm);
+  if (topk_idx) st = enqueue_plan(h, topk_idx, h->comm);
+  if (st == EP_OK) st = cuda_status(enqueue_counts(p));
+  if (st == EP_OK) st = ep_dispatch(h, x, x_dtype, x_scales, H, out_dtype, flags, recv_x, recv_scales, capacity, comm);
+  if (st == EP_OK) st = cuda_status(cudaEventRecord(p->done, h->comm));
+  if (st == EP_OK && !defer_epilogue) st = read_counts(p);
+  if (st != EP_OK) {
+    cudaStreamSynchronize(h->comm);
+    release_pending(p);
+    return st;
+  }
+  *out = p;
+  return EP_OK;
+}
+
+ep_status_t ep_combine_async(ep_handle_t h, const void* y, int64_t y_rows, const float* w, const void* bias,
+                             int64_t H, void* out_dev, ep_stream_t compute_, ep_event_t previous,
+                             int defer_epilogue, ep_pending_t* out) {
+  (void)defer_epilogue;  // a combine has no host-side epilogue: both forms return at once
+  if (!out) return EP_ERR_INVALID;
+  *out = nullptr;
+  if (!h || !y || !w || !out_dev || y_rows < 0 || H < 8 || H % 8 != 0) return EP_ERR_INVALID;
+  if (!aligned(y, 16) || !aligned(out_dev, 16) || !aligned(w, 4) || (bias && !aligned(bias, 16)))
+    return EP_ERR_INVALID;
+  ep_pending_s* p = nullptr;
+  ep_status_t st =
+      begin_async(h, reinterpret_cast<cudaStream_t>(compute_), reinterpret_cast<cudaEvent_t>(previous), false, &p);
+  if (st != EP_OK) return st;
+  st = ep_combine(h, y, y_rows, w, bias, H, out_dev, reinterpret_cast<ep_stream_t>(h->comm));
+  if (st == EP_OK) st = cuda_status(cudaEventRecord(p->done, h->comm));
+  if (st != EP_OK) {
+    cudaStreamSynchronize(h->comm);
+    release_pending(p);
+    return st;
+  }
+  *out = p;
+  return EP_OK;
+}
+
+ep_status_t ep_pending_wait(ep_pending_t p, int64_t* n_exp, int64_t* n_recv) {
+  if (!p) return EP_ERR_INVALID;
+  ep_status_t st = EP_OK;
+  if ((n_exp || n_recv) && p->slot >= 0) st = read_counts(p);
+  const cudaError_t e = cudaStreamWaitEvent(p->compute, p->done, 0);
+  if (st == EP_OK) st = cuda_status(e);
+  if (st == EP_OK && p->have_counts) {
+    if (n_exp) *n_exp = static_cast<int>(p->counts[ep::kSizeExp]);
+    if (n_recv) *n_recv = static_cast<int>(p->counts[ep::kSizeRecv]);
+    st = status_of(p->counts[3]);
+  } else {
+    if (n_exp) *n_exp = 0;
+    if (n_recv) *n_recv = 0;
+  }
+  release_pending(p);
+  return st;
 }
 
 void ep_debug_set_lookback(int64_t poll_limit, int suppress_tile) {

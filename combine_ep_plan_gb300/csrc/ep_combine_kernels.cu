@@ -27,9 +27,12 @@ __device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi) {
 }
 
 // Work item = (token, column chunk of 32*U vectors), so that every warp gets
-// many small items and the kernel has no long tail.
-template <int KMAX, int U, int MINB>
+// many small items and the kernel has no long tail.  PROF: the same kernel,
+// plus a per-CTA record (items, payload bytes, start and end).
+template <int KMAX, int U, int MINB, bool PROF>
 __global__ void __launch_bounds__(256, MINB) ep_combine_kernel(CombineDev c) {
+  unsigned long long t0 = 0, units = 0, bytes = 0;
+  if (PROF && threadIdx.x == 0) t0 = prof_now();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -60,6 +63,14 @@ __global__ void __launch_bounds__(256, MINB) ep_combine_kernel(CombineDev c) {
       row[k] = __shfl_sync(0xffffffffu, my_row, k);
       wk[k] = __shfl_sync(0xffffffffu, my_w, k);
       if (k >= c.K) row[k] = -1;
+    }
+    if (PROF) {  // rows read, the bias row, the output row
+      const int64_t item_bytes = 16 * (hv - v0 < kChunk ? hv - v0 : kChunk);
+      int n = 1 + (c.bias ? 1 : 0);
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) n += row[k] >= 0;
+      ++units;
+      bytes += n * item_bytes;
     }
     uint4 buf[KMAX][U];
 #pragma unroll
@@ -112,9 +123,11 @@ __global__ void __launch_bounds__(256, MINB) ep_combine_kernel(CombineDev c) {
       out[g * hv + v] = o;
     }
   }
+  if (PROF) prof_cta_end(c, c.weights ? kProfCombine : kProfDispatchBackward, t0, 0, 0, 0, units, bytes);
 }
 
-// One full wave of resident CTAs (grid-stride inside).
+// One full wave of resident CTAs (grid-stride inside); under an SM budget,
+// that many SMs' worth.
 template <typename Kernel>
 int resident_grid(Kernel kernel, int threads) {
   int per_sm = 0;
@@ -128,14 +141,23 @@ int resident_grid(Kernel kernel, int threads) {
 #define EP_COMBINE_CTAS_PER_SM 0
 #endif
 
-template <int KMAX, int U, int MINB>
-cudaError_t launch_k(const CombineDev& c, cudaStream_t stream) {
-  static int grid = 0;  // per process; one device type
-  if (grid == 0)
-    grid = EP_COMBINE_CTAS_PER_SM > 0 ? EP_COMBINE_CTAS_PER_SM * num_sms()
-                                      : resident_grid(ep_combine_kernel<KMAX, U, MINB>, 256);
-  ep_combine_kernel<KMAX, U, MINB><<<grid, 256, 0, stream>>>(c);
+template <int KMAX, int U, int MINB, bool PROF>
+cudaError_t launch_kp(const CombineDev& c, cudaStream_t stream, const LaunchCfg& cfg) {
+  static int full = 0;  // per process; one device type
+  auto kernel = ep_combine_kernel<KMAX, U, MINB, PROF>;
+  if (full == 0)
+    full = EP_COMBINE_CTAS_PER_SM > 0 ? EP_COMBINE_CTAS_PER_SM * num_sms() : resident_grid(kernel, 256);
+  long long grid = full;
+  const long long cap = budget_cap(kernel, 256, 0, cfg.sm_budget);
+  if (cap > 0 && grid > cap) grid = cap;
+  kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(c);
+  if (cfg.ctas) *cfg.ctas = grid;
   return cudaGetLastError();
+}
+
+template <int KMAX, int U, int MINB>
+cudaError_t launch_k(const CombineDev& c, cudaStream_t stream, const LaunchCfg& cfg) {
+  return c.prof_rec ? launch_kp<KMAX, U, MINB, true>(c, stream, cfg) : launch_kp<KMAX, U, MINB, false>(c, stream, cfg);
 }
 
 // Combine backward, one CTA of 128 threads per token: grad_out[g] is read
@@ -143,16 +165,16 @@ cudaError_t launch_k(const CombineDev& c, cudaStream_t stream) {
 // <grad_out[g], y[slot]> and grad_y[slot] = bf16(w * grad_out[g]) is written.
 // The dot products are summed per thread over its vectors, then by a fixed
 // shuffle tree per warp and over the four warps in order: deterministic.
-// CTAs beyond T zero the padding rows of grad_y.
+// Items beyond T zero the padding rows of grad_y.  One item per CTA unless
+// an SM budget caps the grid; then CTAs loop over the items.
 template <int KMAX>
-__global__ void __launch_bounds__(128) ep_combine_backward_kernel(CombineBwdDev c) {
+__device__ __forceinline__ void combine_backward_item(const CombineBwdDev& c, int64_t item) {
   constexpr int kWarps = 4;
   __shared__ int s_row[KMAX];
   __shared__ float s_w[KMAX];
   __shared__ float s_dot[kWarps][KMAX];
   const int64_t hv = c.H / 8;
   uint4* gy = static_cast<uint4*>(c.grad_y);
-  const int64_t item = blockIdx.x;
   if (item >= c.T) {
     const int64_t pi = item - c.T;
     if (pi >= c.sizes[kSizePad]) return;
@@ -242,33 +264,46 @@ __global__ void __launch_bounds__(128) ep_combine_backward_kernel(CombineBwdDev 
 }
 
 template <int KMAX>
-cudaError_t launch_bwd(const CombineBwdDev& c, cudaStream_t stream) {
-  const int64_t blocks = c.T + c.max_pad;
+__global__ void __launch_bounds__(128) ep_combine_backward_kernel(CombineBwdDev c) {
+  const int64_t n_items = c.T + c.max_pad;
+  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
+    combine_backward_item<KMAX>(c, item);
+    __syncthreads();  // the next item reuses the shared slots
+  }
+}
+
+template <int KMAX>
+cudaError_t launch_bwd(const CombineBwdDev& c, cudaStream_t stream, const LaunchCfg& cfg) {
+  long long blocks = c.T + c.max_pad;
+  const long long cap = budget_cap(ep_combine_backward_kernel<KMAX>, 128, 0, cfg.sm_budget);
+  if (cap > 0 && blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
   ep_combine_backward_kernel<KMAX><<<static_cast<unsigned>(blocks), 128, 0, stream>>>(c);
+  if (cfg.ctas) *cfg.ctas = blocks;
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_combine_backward(const CombineBwdDev& c, cudaStream_t stream) {
-  if (c.K <= 2) return launch_bwd<2>(c, stream);
-  if (c.K <= 4) return launch_bwd<4>(c, stream);
-  if (c.K <= 6) return launch_bwd<6>(c, stream);
-  if (c.K <= 8) return launch_bwd<8>(c, stream);
-  return launch_bwd<16>(c, stream);
+cudaError_t launch_combine_backward(const CombineBwdDev& c, cudaStream_t stream, const LaunchCfg& cfg) {
+  if (c.K <= 2) return launch_bwd<2>(c, stream, cfg);
+  if (c.K <= 4) return launch_bwd<4>(c, stream, cfg);
+  if (c.K <= 6) return launch_bwd<6>(c, stream, cfg);
+  if (c.K <= 8) return launch_bwd<8>(c, stream, cfg);
+  return launch_bwd<16>(c, stream, cfg);
 }
 
-cudaError_t launch_combine(const CombineDev& c, cudaStream_t stream) {
+cudaError_t launch_combine(const CombineDev& c, cudaStream_t stream, const LaunchCfg& cfg) {
   switch (c.K) {
-    case 1: return launch_k<1, 4, 4>(c, stream);
-    case 2: return launch_k<2, 2, 4>(c, stream);
-    case 3: return launch_k<3, 2, 4>(c, stream);
-    case 4: return launch_k<4, 1, 4>(c, stream);
-    case 5: return launch_k<5, 1, 4>(c, stream);
-    case 6: return launch_k<6, 1, 4>(c, stream);
-    case 7: return launch_k<7, 1, 3>(c, stream);
-    case 8: return launch_k<8, 1, 3>(c, stream);
-    default: return launch_k<16, 1, 1>(c, stream);
+    case 1: return launch_k<1, 4, 4>(c, stream, cfg);
+    case 2: return launch_k<2, 2, 4>(c, stream, cfg);
+    case 3: return launch_k<3, 2, 4>(c, stream, cfg);
+    case 4: return launch_k<4, 1, 4>(c, stream, cfg);
+    case 5: return launch_k<5, 1, 4>(c, stream, cfg);
+    case 6: return launch_k<6, 1, 4>(c, stream, cfg);
+    case 7: return launch_k<7, 1, 3>(c, stream, cfg);
+    case 8: return launch_k<8, 1, 3>(c, stream, cfg);
+    default: return launch_k<16, 1, 1>(c, stream, cfg);
   }
 }
 

@@ -42,9 +42,12 @@ __device__ __forceinline__ int64_t scale_at(const DispatchDev& a, int64_t r, int
 
 // Copies whole rows: BF16 hidden rows (row_vec = H/8 vectors), or E4M3 codes
 // of pre-quantised input (row_vec = H/16) together with their H/128 fp32
-// scales, which the warp owning chunk 0 of a row copies.
-template <int ROW_DIV, bool WITH_SCALES>
+// scales, which the warp owning chunk 0 of a row copies.  PROF: the same
+// kernel, plus a per-CTA record (items, payload bytes, start and end).
+template <int ROW_DIV, bool WITH_SCALES, bool PROF>
 __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
+  unsigned long long t0 = 0, units = 0, bytes = 0;
+  if (PROF && threadIdx.x == 0) t0 = prof_now();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -60,6 +63,11 @@ __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
   for (int64_t item = warp; item < n_items; item += nwarps) {
     const int64_t ri = item / chunks;
     const int64_t v0 = (item - ri * chunks) * kChunk;
+    // payload bytes of this item's part of one row (codes or bf16), and of
+    // its scales (chunk 0 only)
+    const int64_t item_bytes = 16 * (hv - v0 < kChunk ? hv - v0 : kChunk);
+    const int64_t scale_bytes = (WITH_SCALES && v0 == 0) ? 4 * groups : 0;
+    if (PROF) ++units;
     if (ri < a.T) {
       const int64_t g = ri;
       int my_row = -1;
@@ -76,9 +84,11 @@ __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
         if (v < hv) buf[u] = ld_stream(src + v);
       }
       const bool copy_scales = WITH_SCALES && v0 == 0;
+      if (PROF) bytes += item_bytes + scale_bytes;
       for (int k = 0; k < a.K; ++k) {
         const int r = __shfl_sync(0xffffffffu, my_row, k);
         if (r < 0) continue;
+        if (PROF) bytes += item_bytes + scale_bytes;
         uint4* dst = out + static_cast<int64_t>(r) * hv;
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
@@ -94,6 +104,7 @@ __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
         if (lane == 0) atomicOr(a.status, kStCapacity);
         continue;
       }
+      if (PROF) bytes += item_bytes + scale_bytes;
       uint4* dst = out + static_cast<int64_t>(r) * hv;
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -105,6 +116,8 @@ __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
         for (int64_t j = lane; j < groups; j += 32) a.scales[scale_at(a, r, j, groups)] = 0.0f;
     }
   }
+  if (PROF)
+    prof_cta_end(a, ROW_DIV == 8 ? kProfDispatchBf16 : kProfDispatchFp8Input, t0, 0, 0, 0, units, bytes);
 }
 
 // Two fp32 values -> two E4M3 codes (lo in the low byte), RNE, satfinite.
@@ -150,7 +163,10 @@ __device__ __forceinline__ float bf16_hi(unsigned w) { return __uint_as_float(w 
 #endif
 constexpr int kFp8Units = EP_FP8_UNITS;
 
+template <bool PROF>
 __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
+  unsigned long long t0 = 0, units = 0, bytes = 0;
+  if (PROF && threadIdx.x == 0) t0 = prof_now();
   const int lane = threadIdx.x & 31;
   const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
@@ -172,6 +188,11 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
     // lanes 0 .. 4*kFp8Units-1 own the chunk's scales, in order
     const int sc_lane = lane < 4 * kFp8Units ? lane : 0;
     const bool sc_active = lane < 4 * kFp8Units && g_base + lane < groups;
+    // payload of the item: 32 bytes of bf16 in, 16 bytes of codes out per
+    // 16-element unit, and 4 bytes per scale written
+    const int64_t n_q = qv - q_base < kChunkVec ? qv - q_base : kChunkVec;
+    const int64_t n_g = groups - g_base < 4 * kFp8Units ? groups - g_base : 4 * kFp8Units;
+    if (PROF) ++units;
     if (ri < a.T) {
       const int64_t g = ri;
       int my_row = -1;
@@ -237,9 +258,11 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
         const float v = __shfl_sync(0xffffffffu, scale_u[u], (sc_lane & 3) * 8);
         if ((sc_lane >> 2) == u) my_scale = v;
       }
+      if (PROF) bytes += 32 * n_q;
       for (int k = 0; k < a.K; ++k) {
         const int r = __shfl_sync(0xffffffffu, my_row, k);
         if (r < 0) continue;
+        if (PROF) bytes += 16 * n_q + 4 * n_g;
         uint4* dst = out + static_cast<int64_t>(r) * qv;
 #pragma unroll
         for (int u = 0; u < kFp8Units; ++u) {
@@ -254,6 +277,7 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
         if (lane == 0) atomicOr(a.status, kStCapacity);
         continue;
       }
+      if (PROF) bytes += 16 * n_q + 4 * n_g;
       uint4* dst = out + static_cast<int64_t>(r) * qv;
 #pragma unroll
       for (int u = 0; u < kFp8Units; ++u) {
@@ -263,30 +287,44 @@ __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
       if (sc_active) a.scales[scale_at(a, r, g_base + lane, groups)] = 0.0f;
     }
   }
+  if (PROF) prof_cta_end(a, kProfDispatchFp8, t0, 0, 0, 0, units, bytes);
 }
 
 // One warp per work item: the grid covers the worst-case item count (T rows
 // plus E*(A-1) padding rows, in chunks); warps without an item exit at once.
 // Many short-lived CTAs, balanced by the hardware block scheduler, keep more
-// stores in flight than a resident grid looping over the items.
-unsigned item_grid(int64_t rows, int64_t chunks) {
+// stores in flight than a resident grid looping over the items.  Under an
+// SM budget the grid is capped at that many SMs' worth of resident CTAs,
+// which then loop over the items.
+long long item_grid(int64_t rows, int64_t chunks) {
   const int64_t warps = rows * chunks;
   const int64_t blocks = (warps + 7) / 8;
-  return static_cast<unsigned>(blocks < 1 ? 1 : (blocks > 0x7fffffff ? 0x7fffffff : blocks));
+  return blocks < 1 ? 1 : (blocks > 0x7fffffff ? 0x7fffffff : blocks);
+}
+
+template <typename Kernel>
+cudaError_t launch_items(Kernel kernel, const DispatchDev& d, int64_t chunks, cudaStream_t stream,
+                         const LaunchCfg& cfg) {
+  long long grid = item_grid(d.T + d.max_pad, chunks);
+  const long long cap = budget_cap(kernel, 256, 0, cfg.sm_budget);
+  if (cap > 0 && grid > cap) grid = cap;
+  kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(d);
+  if (cfg.ctas) *cfg.ctas = grid;
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_dispatch_bf16(const DispatchDev& d, cudaStream_t stream) {
+cudaError_t launch_dispatch_bf16(const DispatchDev& d, cudaStream_t stream, const LaunchCfg& cfg) {
   const int64_t chunks = (d.H / 8 + 32 * kUnroll - 1) / (32 * kUnroll);
-  ep_dispatch_copy_kernel<8, false><<<item_grid(d.T + d.max_pad, chunks), 256, 0, stream>>>(d);
-  return cudaGetLastError();
+  if (d.prof_rec) return launch_items(ep_dispatch_copy_kernel<8, false, true>, d, chunks, stream, cfg);
+  return launch_items(ep_dispatch_copy_kernel<8, false, false>, d, chunks, stream, cfg);
 }
 
-cudaError_t launch_dispatch_fp8_input(const DispatchDev& d, cudaStream_t stream) {
+cudaError_t launch_dispatch_fp8_input(const DispatchDev& d, cudaStream_t stream, const LaunchCfg& cfg) {
   const int64_t chunks = (d.H / 16 + 32 * kUnroll - 1) / (32 * kUnroll);
-  ep_dispatch_copy_kernel<16, true><<<item_grid(d.T + d.max_pad, chunks), 256, 0, stream>>>(d);
-  return cudaGetLastError();
+  if (d.prof_rec) return launch_items(ep_dispatch_copy_kernel<16, true, true>, d, chunks, stream, cfg);
+  return launch_items(ep_dispatch_copy_kernel<16, true, false>, d, chunks, stream, cfg);
 }
 
 namespace {
@@ -328,10 +366,10 @@ cudaError_t launch_dispatch_metadata(const MetaDev& m, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_dispatch_fp8(const DispatchDev& d, cudaStream_t stream) {
+cudaError_t launch_dispatch_fp8(const DispatchDev& d, cudaStream_t stream, const LaunchCfg& cfg) {
   const int64_t chunks = (d.H / 16 + 32 * kFp8Units - 1) / (32 * kFp8Units);
-  ep_dispatch_fp8_kernel<<<item_grid(d.T + d.max_pad, chunks), 256, 0, stream>>>(d);
-  return cudaGetLastError();
+  if (d.prof_rec) return launch_items(ep_dispatch_fp8_kernel<true>, d, chunks, stream, cfg);
+  return launch_items(ep_dispatch_fp8_kernel<false>, d, chunks, stream, cfg);
 }
 
 }  // namespace ep

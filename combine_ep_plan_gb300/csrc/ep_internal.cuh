@@ -31,6 +31,89 @@ constexpr int kSizeExp = 1;   // N_exp
 constexpr int kSizePad = 2;   // N_pad
 constexpr int kSizeWords = 4;
 
+// Per-CTA profile records, a compile-time switch: only the PROF
+// instantiations of the plan, dispatch and combine kernels write one, so the
+// default kernels carry no profiling code at all.  Each CTA owns one record
+// of kProfWords words (no atomics); the host reads the buffer once.
+//   [0] kernel id << 56 | launch sequence << 32 | CTA index
+//   [1] start  [2..4] stage marks (kernel specific, 0 if unused)  [5] end
+//       (global timer, ns)
+//   [6] work units  [7] payload bytes read + written
+constexpr int kProfWords = 8;
+enum : unsigned {
+  kProfPlan = 1,
+  kProfDispatchBf16 = 2,
+  kProfDispatchFp8 = 3,
+  kProfDispatchFp8Input = 4,
+  kProfCombine = 5,
+  kProfDispatchBackward = 6,
+};
+// The record target travels in each kernel's parameter struct as two plain
+// fields (the copy kernel's parameters stay within 128 bytes; beyond that it
+// needed more registers):
+//   prof_rec   this launch's first record, NULL when profiling is off
+//   prof_meta  launch sequence (24 bits) << 40 | records available
+#define EP_PROF_FIELDS          \
+  unsigned long long* prof_rec; \
+  long long prof_meta
+constexpr int kProfAvailBits = 40;
+
+__device__ __forceinline__ unsigned long long prof_now() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Written by thread 0 of the CTA; records past the buffer are dropped.
+template <class Dev>
+__device__ __forceinline__ void prof_write(const Dev& d, unsigned kind, unsigned long long t0,
+                                           unsigned long long ta, unsigned long long tb, unsigned long long tc,
+                                           unsigned long long t_end, unsigned long long units,
+                                           unsigned long long bytes) {
+  const long long avail = d.prof_meta & ((1ll << kProfAvailBits) - 1);
+  const unsigned long long seq = static_cast<unsigned long long>(d.prof_meta) >> kProfAvailBits;
+  if (d.prof_rec == nullptr || static_cast<long long>(blockIdx.x) >= avail) return;
+  unsigned long long* r = d.prof_rec + static_cast<long long>(blockIdx.x) * kProfWords;
+  r[0] = (static_cast<unsigned long long>(kind) << 56) | ((seq & 0xffffffu) << 32) | blockIdx.x;
+  r[1] = t0;
+  r[2] = ta;
+  r[3] = tb;
+  r[4] = tc;
+  r[5] = t_end;
+  r[6] = units;
+  r[7] = bytes;
+}
+
+// End of a profiled CTA, called by all its threads: sums the warp-uniform
+// counters over the CTA's warps; thread 0 writes the record.
+template <class Dev>
+__device__ __forceinline__ void prof_cta_end(const Dev& d, unsigned kind, unsigned long long t0,
+                                             unsigned long long ta, unsigned long long tb, unsigned long long tc,
+                                             unsigned long long units, unsigned long long bytes) {
+  __shared__ unsigned long long s_units[32], s_bytes[32];
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    s_units[warp] = units;
+    s_bytes[warp] = bytes;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long u = 0, b = 0;
+    for (int w = 0; w < static_cast<int>((blockDim.x + 31) >> 5); ++w) {
+      u += s_units[w];
+      b += s_bytes[w];
+    }
+    prof_write(d, kind, t0, ta, tb, tc, prof_now(), u, b);
+  }
+}
+
+// How a launch is shaped: an SM budget (0 = the whole device), and where
+// the launcher reports the CTAs it launched (the profile record cursor).
+struct LaunchCfg {
+  int sm_budget = 0;
+  long long* ctas = nullptr;
+};
+
 // Look-back descriptor: high 32 bits = (plan epoch << 2) | state, low 32
 // bits = value.
 constexpr unsigned long long kDescAggregate = 1ull;
@@ -72,10 +155,11 @@ struct PlanDev {
   // bounded wait of the look-back, and a test hook
   long long poll_limit;
   int suppress_tile;
+  EP_PROF_FIELDS;
 };
 
 // Host-side launchers (defined in the .cu files, called by the C ABI layer).
-cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream);
+cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream, const LaunchCfg& cfg);
 size_t plan_smem_bytes(int P, int E, int K);
 
 struct DispatchDev {
@@ -94,10 +178,11 @@ struct DispatchDev {
   int64_t max_pad;        // upper bound of N_pad: E*(A-1) (sizes the grid)
   int zero_pad;
   int scales_col_major;   // scales stored [H/128][capacity] instead of [capacity][H/128]
+  EP_PROF_FIELDS;
 };
-cudaError_t launch_dispatch_bf16(const DispatchDev& d, cudaStream_t stream);
-cudaError_t launch_dispatch_fp8(const DispatchDev& d, cudaStream_t stream);
-cudaError_t launch_dispatch_fp8_input(const DispatchDev& d, cudaStream_t stream);
+cudaError_t launch_dispatch_bf16(const DispatchDev& d, cudaStream_t stream, const LaunchCfg& cfg);
+cudaError_t launch_dispatch_fp8(const DispatchDev& d, cudaStream_t stream, const LaunchCfg& cfg);
+cudaError_t launch_dispatch_fp8_input(const DispatchDev& d, cudaStream_t stream, const LaunchCfg& cfg);
 
 struct MetaDev {
   const int* slot;        // [T,K]
@@ -125,8 +210,9 @@ struct CombineDev {
   int K;
   int64_t H;
   int64_t y_rows;
+  EP_PROF_FIELDS;
 };
-cudaError_t launch_combine(const CombineDev& c, cudaStream_t stream);
+cudaError_t launch_combine(const CombineDev& c, cudaStream_t stream, const LaunchCfg& cfg);
 
 struct CombineBwdDev {
   const void* grad_out;   // [T,H] bf16
@@ -145,8 +231,18 @@ struct CombineBwdDev {
   int64_t grad_y_rows;
   int64_t max_pad;        // upper bound of N_pad, 0 without zero padding
 };
-cudaError_t launch_combine_backward(const CombineBwdDev& c, cudaStream_t stream);
+cudaError_t launch_combine_backward(const CombineBwdDev& c, cudaStream_t stream, const LaunchCfg& cfg);
 
 int num_sms();
+
+// At most `budget` SMs' worth of resident CTAs (budget 0: no cap).
+template <typename Kernel>
+long long budget_cap(Kernel kernel, int threads, size_t smem, int budget) {
+  if (budget <= 0) return -1;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  return static_cast<long long>(per_sm) * budget;
+}
 
 }  // namespace ep

@@ -272,8 +272,14 @@ __device__ void offsets_warp_scan(const PlanDev& p, int* exp_off, int* pad_off, 
   }
 }
 
+// PROF: the same kernel, plus a per-CTA record: marks after the route scan
+// of its last tile, at the end of phase 1 and past the grid barrier; the
+// tokens it scanned.
+template <bool PROF>
 __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   extern __shared__ __align__(16) uint32_t smem[];
+  unsigned long long t_start = 0, t_scan = 0, t_phase1 = 0, t_barrier = 0, scanned = 0;
+  if (PROF && threadIdx.x == 0) t_start = prof_now();
 
   // ---------------- phase 1: tiles ----------------
   uint32_t* bits = smem;                                           // [kTileWords * ncols]
@@ -286,6 +292,10 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
     __syncthreads();
     build_tile_bits(p, ids, bits);
     __syncthreads();
+    if (PROF && threadIdx.x == 0) {
+      t_scan = prof_now();
+      scanned += static_cast<unsigned long long>(min64(kTile, p.T - t0));
+    }
     uint32_t* g_bits = p.tile_bits + static_cast<int64_t>(tile) * kTileWords * p.ncols;
     int* g_wpre = p.tile_wpre + static_cast<int64_t>(tile) * kTileWords * p.ncols;
     for (int i = threadIdx.x; i < kTileWords * p.ncols; i += blockDim.x) g_bits[i] = bits[i];
@@ -313,11 +323,13 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
     __syncthreads();  // before the next tile reuses shared memory
   }
   if (timed_out) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
+  if (PROF && threadIdx.x == 0) t_phase1 = prof_now();
 
   if (!grid_sync(p)) {
     if (threadIdx.x == 0) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
     return;
   }
+  if (PROF && threadIdx.x == 0) t_barrier = prof_now();
 
   // ---------------- phase 2: every plan array, all CTAs ----------------
   int* exp_off = reinterpret_cast<int*>(smem);  // [E+1]
@@ -461,6 +473,7 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
     p.pad_rows[i] = row;
     p.exp_src[row] = -1;
   }
+  if (PROF) prof_cta_end(p, kProfPlan, t_start, t_scan, t_phase1, t_barrier, scanned, 0);
 }
 
 }  // namespace
@@ -471,42 +484,55 @@ size_t plan_smem_bytes(int P, int E, int K) {
   return phase1 > phase2 ? phase1 : phase2;
 }
 
-// Co-resident CTAs (at most two per SM, which keeps the grid barrier cheap),
-// and no more than the plan's work needs: one CTA per tile at least, and
-// about one CTA per 1024 phase-2 outputs.
-int plan_grid(const PlanDev& p) {
+namespace {
+
+// Co-resident CTAs (at most two per SM, which keeps the grid barrier cheap;
+// under an SM budget, two per budgeted SM), and no more than the plan's work
+// needs: one CTA per tile at least, and about one CTA per 1024 phase-2
+// outputs.  Phase 1 loops over the tiles when the grid is smaller.
+template <bool PROF>
+int plan_grid(const PlanDev& p, int sm_budget) {
   const size_t smem = plan_smem_bytes(p.P, p.E, p.K);
   static size_t cached_smem = ~static_cast<size_t>(0);
-  static int cached_cap = 0;
+  static int cached_per_sm = 0;
   if (smem != cached_smem) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_plan_kernel, kTile, smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_plan_kernel<PROF>, kTile, smem) != cudaSuccess ||
         per_sm < 1)
       return 0;
-    if (per_sm > 2) per_sm = 2;
-    cached_cap = per_sm * num_sms();
+    cached_per_sm = per_sm > 2 ? 2 : per_sm;
     cached_smem = smem;
   }
+  const int sms = sm_budget > 0 && sm_budget < num_sms() ? sm_budget : num_sms();
+  const int64_t cap = static_cast<int64_t>(cached_per_sm) * sms;
   const int64_t work = p.T * (p.K + p.P) + static_cast<int64_t>(p.P) * p.P * p.C + static_cast<int64_t>(p.P) * p.E;
   int64_t grid = (work + 1023) / 1024;
   if (grid < p.num_tiles) grid = p.num_tiles;
-  if (grid > cached_cap) grid = cached_cap;
+  if (grid > cap) grid = cap;
   return static_cast<int>(grid);
 }
 
-cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream) {
+template <bool PROF>
+cudaError_t launch_plan_t(const PlanDev& p, cudaStream_t stream, const LaunchCfg& cfg) {
   const size_t smem = plan_smem_bytes(p.P, p.E, p.K);
   if (smem > 48 * 1024) {
-    cudaError_t err = cudaFuncSetAttribute(ep_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(ep_plan_kernel<PROF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
   }
-  const int grid = plan_grid(p);
+  const int grid = plan_grid<PROF>(p, cfg.sm_budget);
   if (grid < 1) return cudaErrorInvalidConfiguration;
   PlanDev arg = p;
   void* args[] = {&arg};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(ep_plan_kernel), dim3(grid), dim3(kTile),
+  if (cfg.ctas) *cfg.ctas = grid;
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(ep_plan_kernel<PROF>), dim3(grid), dim3(kTile),
                                      args, smem, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream, const LaunchCfg& cfg) {
+  return p.prof_rec ? launch_plan_t<true>(p, stream, cfg) : launch_plan_t<false>(p, stream, cfg);
 }
 
 }  // namespace ep

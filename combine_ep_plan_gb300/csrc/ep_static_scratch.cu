@@ -139,7 +139,7 @@ extern "C" ep_status_t ep_plan_static_scratch(const int64_t* topk_idx, int64_t S
   p.poll_limit = 1ll << 20;
   p.suppress_tile = -1;
 
-  e = ep::launch_plan(p, stream);
+  e = ep::launch_plan(p, stream, ep::LaunchCfg{});
   if (e != cudaSuccess) return to_status(e);
 
   // Totals, sizes and the status word leave the scratch for the caller.

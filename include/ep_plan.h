@@ -41,6 +41,13 @@ typedef struct CUstream_st *ep_stream_t;
 
 typedef struct ep_handle_s *ep_handle_t;
 
+/* Same underlying type as cudaEvent_t. */
+struct CUevent_st;
+typedef struct CUevent_st *ep_event_t;
+
+/* An issued asynchronous dispatch or combine (see ep_dispatch_async). */
+typedef struct ep_pending_s *ep_pending_t;
+
 typedef enum {
     EP_OK = 0,
     EP_ERR_INVALID = 1,  /* bad argument, or routing data the method rejects */
@@ -307,7 +314,10 @@ ep_status_t ep_handle_info(ep_handle_t handle, int64_t *num_tokens_per_rank, int
 
 /*
  * ep_handle_destroy — release the handle.  Its device memory is freed in
- * stream order on `stream` (after work already enqueued there).
+ * stream order on `stream` (after work already enqueued there).  If the
+ * handle issued asynchronous calls, this synchronises its communication
+ * stream first.  EP_ERR_INVALID, and nothing released, while a pending
+ * object of the handle has not been waited on.
  */
 ep_status_t ep_handle_destroy(ep_handle_t handle, ep_stream_t stream);
 
@@ -369,6 +379,104 @@ ep_status_t ep_plan_static_scratch(const int64_t *topk_idx_dev, int64_t num_toke
                                    int num_ranks, int num_topk, int num_experts,
                                    int expert_alignment, int num_channels,
                                    const ep_plan_buffers_t *out_dev_buffers, ep_stream_t stream);
+
+/*
+ * ep_set_num_sms — SM budget of the handle's kernels ([TT] §3.3: num_sms,
+ * which cached dispatch and combine take from the handle).  num_sms = 0 (the
+ * default) or at least the device's SM count: every launch may use the whole
+ * device.  Otherwise the plan, dispatch, combine and backward launches made
+ * with this handle use grids of at most num_sms SMs' worth of resident CTAs,
+ * which loop over the work, so that other kernels running at the same time
+ * (an overlapped shared expert) keep the remaining SMs.  Results do not
+ * depend on the budget.  EP_ERR_INVALID for num_sms < 0.
+ */
+ep_status_t ep_set_num_sms(ep_handle_t handle, int num_sms);
+
+/*
+ * ep_dispatch_async / ep_combine_async / ep_pending_wait — issue now, finish
+ * later ([TT] §3.4 defer_epilogue + async_with_compute_stream, §4.4 why the
+ * dispatch epilogue can be deferred).
+ *
+ * The work is enqueued on the handle's communication stream (a non-blocking
+ * stream the handle creates on first use, on the handle's device, which must
+ * be current) and the call returns a pending object.  That stream first
+ * waits for `previous` (an event the caller recorded on its compute stream
+ * once the inputs were ready), or, with previous = NULL, for all work
+ * enqueued on compute_stream before the call.  Meanwhile the compute stream
+ * is free for independent work; ep_set_num_sms leaves it SMs to run on.
+ *
+ * Dispatch: topk_idx_dev non-NULL re-plans the handle first (ep_replan on the
+ * communication stream: a fresh dispatch); NULL dispatches with the
+ * handle's current plan (a cached dispatch).  The other arguments are those
+ * of ep_dispatch.  On one device the rows land in recv_x_dev during the
+ * issue; what the method's epilogue adds is the exact receive counts the
+ * caller sizes its tensors by.  The device copies the counts (and the status
+ * word) to pinned host memory right after the plan, before the row scatter.
+ *   defer_epilogue = 0: the call waits on the host for those counts (the plan
+ *                       only; the scatter keeps running) before it returns.
+ *   defer_epilogue = 1: the call returns at once; the counts are read when
+ *                       ep_pending_wait asks for them.
+ * At most 8 dispatches of one handle may be pending: the 9th returns
+ * EP_ERR_CAPACITY before enqueuing anything.
+ *
+ * Combine: the arguments are those of ep_combine.  A combine has no host-side
+ * epilogue: both values of defer_epilogue return at once.
+ *
+ * ep_pending_wait — makes compute_stream wait (on the device, no host
+ * block) for all the issued work, then frees the pending object; results are
+ * usable in compute-stream order afterwards.  num_expanded_host /
+ * num_recv_host (may be NULL) receive N_exp and N_recv of a dispatch (0 for a
+ * combine); asking for them makes a deferred dispatch wait on the host for
+ * the plan.  Returns the status the device recorded up to the plan (an
+ * invalid expert id, a look-back timeout) when the counts were read, else
+ * EP_OK; later device errors (a capacity overflow in the scatter) are
+ * returned by the next ep_sync_status.  Every pending object must be waited
+ * on exactly once, before its handle is destroyed, and the buffers it uses
+ * must stay allocated until then.
+ */
+ep_status_t ep_dispatch_async(ep_handle_t handle, const int64_t *topk_idx_dev, const void *x_dev,
+                              ep_dtype_t x_dtype, const float *x_scales_dev, int64_t hidden,
+                              ep_dtype_t out_dtype, int flags, void *recv_x_dev,
+                              float *recv_scales_dev, int64_t capacity_rows,
+                              ep_stream_t compute_stream, ep_event_t previous,
+                              int defer_epilogue, ep_pending_t *pending_host);
+
+ep_status_t ep_combine_async(ep_handle_t handle, const void *y_dev, int64_t y_rows,
+                             const float *topk_weights_dev, const void *bias_dev, int64_t hidden,
+                             void *out_dev, ep_stream_t compute_stream, ep_event_t previous,
+                             int defer_epilogue, ep_pending_t *pending_host);
+
+ep_status_t ep_pending_wait(ep_pending_t pending, int64_t *num_expanded_host,
+                            int64_t *num_recv_host);
+
+/*
+ * ep_profile_begin / ep_profile_end — per-CTA profile records ([DO] "Device
+ * 侧计时": stage times and bytes per core, each core writing its own slot,
+ * no atomics, read by the host once).  The records come from separate
+ * instantiations of the kernels that the library launches only while
+ * profiling is on, so the default kernels carry no profiling code.
+ *
+ * Between begin and end, every plan, dispatch, combine and dispatch-backward
+ * launch of this handle writes one record per CTA into records_dev (device,
+ * 8-byte aligned, capacity_records records of 8 uint64 each), in launch order;
+ * records that do not fit are dropped.  Outputs are identical to unprofiled
+ * launches.  The combine backward writes none.  Record layout:
+ *   [0] kernel << 56 | launch sequence (24 bits) << 32 | CTA index; kernel
+ *       1 plan, 2 BF16 dispatch, 3 FP8 dispatch (quantising), 4 dispatch of
+ *       pre-quantised FP8, 5 combine, 6 dispatch backward
+ *   [1] start, [5] end: device global timer, ns
+ *   [2] [3] [4] stage marks (plan: route scan of the CTA's last tile done,
+ *       phase 1 done, grid barrier passed; 0 for the other kernels)
+ *   [6] work units: plan, tokens scanned; others, (row, column chunk) items
+ *   [7] payload bytes read and written by the CTA (hidden rows, codes, scales,
+ *       bias; 0 for the plan)
+ * ep_profile_end stops recording and returns how many records were written
+ * and dropped (either pointer may be NULL); read the records after
+ * synchronising the streams the launches ran on.
+ */
+ep_status_t ep_profile_begin(ep_handle_t handle, uint64_t *records_dev, int64_t capacity_records);
+ep_status_t ep_profile_end(ep_handle_t handle, int64_t *records_written_host,
+                           int64_t *records_dropped_host);
 
 /*
  * ep_debug_set_lookback — test hook for the bounded wait of the plan's

@@ -34,14 +34,16 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for required in ["ep_plan", "ep_dispatch", "ep_combine", "ep_dispatch_cached", "ep_dispatch_fresh",
-                     "ep_plan_sizes", "ep_handle_destroy", "ep_handle_get"]:
+                     "ep_plan_sizes", "ep_handle_destroy", "ep_handle_get", "ep_set_num_sms",
+                     "ep_dispatch_async", "ep_combine_async", "ep_pending_wait", "ep_profile_begin",
+                     "ep_profile_end"]:
         assert required in names
 
 
 def test_every_declared_symbol_is_exported(lib):
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
-    assert lib.ep_abi_version() == 2
+    assert lib.ep_abi_version() == 3
 
 
 def test_status_strings(lib):
@@ -108,3 +110,20 @@ def test_calls_on_null_handle_are_rejected(lib):
         assert lib.ep_dispatch_fresh(FAKE, 64, 4, 2, 8, 1, 0, x, xd, xs, H, od, fl, rx, rs, 10, None,
                                      ctypes.byref(h)) == ep.EP_ERR_INVALID
     assert not h.value
+
+
+def test_async_profile_and_budget_calls_reject_bad_arguments(lib):
+    p = ctypes.c_void_p(123)
+    assert lib.ep_dispatch_async(None, None, FAKE, 0, None, 256, 0, 1, FAKE, None, 10, None, None, 1,
+                                 ctypes.byref(p)) == ep.EP_ERR_INVALID
+    assert not p.value
+    assert lib.ep_dispatch_async(None, None, FAKE, 0, None, 256, 0, 1, FAKE, None, 10, None, None, 1,
+                                 None) == ep.EP_ERR_INVALID
+    p = ctypes.c_void_p(123)
+    assert lib.ep_combine_async(None, FAKE, 10, FAKE, None, 256, FAKE, None, None, 0,
+                                ctypes.byref(p)) == ep.EP_ERR_INVALID
+    assert not p.value
+    assert lib.ep_pending_wait(None, None, None) == ep.EP_ERR_INVALID
+    assert lib.ep_set_num_sms(None, 4) == ep.EP_ERR_INVALID
+    assert lib.ep_profile_begin(None, FAKE, 16) == ep.EP_ERR_INVALID
+    assert lib.ep_profile_end(None, None, None) == ep.EP_ERR_INVALID
