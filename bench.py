@@ -400,7 +400,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # Per-phase kernel times come from events recorded between the kernels of
+    # every 4th timed step.  An event between two kernels serialises them (the
+    # next launch can no longer overlap the end of the previous grid), so the
+    # other steps carry none.
+    every = 4
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] if i % every == 0 else None
+              for i in range(args.steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     t_wall0 = time.time()
@@ -413,9 +419,10 @@ def run_ours(args):
     barrier()
     sampler.mark(t_wall0, t_wall1)
     local_ms = start.elapsed_time(end)
-    plan_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
-    disp_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events) / (1 + w.cached_steps)
-    comb_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in events)
+    sampled = [e for e in events if e is not None]
+    plan_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in sampled)
+    disp_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in sampled) / (1 + w.cached_steps)
+    comb_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in sampled)
     agg = aggregate(led["total"], w.T, local_ms, world, args.steps)
 
     # End to end through the public API with host buffers: every step copies
@@ -510,6 +517,10 @@ def run_ours(args):
                "sample": f"full {w.name} workload (T={w.T}, H={w.H}), {s['passes']} pass(es) of the step, "
                          f"single-threaded C oracle", "tokens_per_s": round(s["tokens_per_s"], 1)}
 
+    overlap = run_overlap(ep, w, idx_t, x_t, wts_t, stream, args) if args.overlap else None
+    cta_profile = run_cta_profile(ep, w, idx_t, x_t, wts_t, y, stream, recv, recv_sc, out_dtype) \
+        if args.cta_profile else None
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(agg["gbs"], 2), "unit": "GB/s", "n_gpus": world,
@@ -519,7 +530,8 @@ def run_ours(args):
             "tokens_per_s": round(agg["tokens_per_s"], 1),
             "hbm_roofline_frac": round(agg["gbs"] / world / peak, 4),
             "config": workload_config(w),
-            "phases_ms": {"plan": round(plan_ms, 5), "dispatch": round(disp_ms, 5), "combine": round(comb_ms, 5)},
+            "phases_ms": {"plan": round(plan_ms, 5), "dispatch": round(disp_ms, 5), "combine": round(comb_ms, 5),
+                          "sampled_steps": len(sampled)},
             "ledger_bytes_per_step": led,
             "payload_gbs": round(world * payload_ledger(w, n_recv) / (agg["ms_per_step"] / 1e3) / 1e9, 2),
             "roofline": roofline,
@@ -533,9 +545,109 @@ def run_ours(args):
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
+        if overlap is not None:
+            line["overlap"] = overlap
+        if cta_profile is not None:
+            line["cta_profile"] = cta_profile
         print(json.dumps(line), flush=True)
     barrier()
     return 0
+
+
+def run_overlap(ep, w, idx_t, x_t, wts_t, stream, args):
+    """The pattern of an overlapped shared expert: a fresh dispatch issued on
+    the handle's communication stream under an SM budget while a shared-expert
+    FFN (two bf16 GEMMs, hidden -> 2048 -> hidden, through torch) runs on the
+    compute stream; then the combine adds the shared output as its bias.
+    Times per step: both in series on one stream, and overlapped, for several
+    SM budgets, plus each part alone."""
+    import torch
+    F = 2048
+    g = torch.Generator(device=x_t.device).manual_seed(11)
+    w_up = (torch.randn((w.H, F), device=x_t.device, generator=g) / w.H ** 0.5).to(torch.bfloat16)
+    w_down = (torch.randn((F, w.H), device=x_t.device, generator=g) / F ** 0.5).to(torch.bfloat16)
+    cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
+    recv = torch.empty((cap, w.H), dtype=torch.bfloat16, device=x_t.device)
+    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=x_t.device)
+    hid = torch.empty((w.T, F), dtype=torch.bfloat16, device=x_t.device)
+    shared = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=x_t.device)
+    h = ep.plan(idx_t, w.P, w.E, w.A, stream=stream)
+
+    def shared_expert():
+        torch.matmul(x_t, w_up, out=hid)
+        torch.matmul(hid, w_down, out=shared)
+
+    def serial():
+        h.replan(idx_t, stream=stream)
+        ep.dispatch(h, x_t, "bf16", True, recv_x=recv, stream=stream)
+        shared_expert()
+        ep.combine(h, recv, wts_t, out=out, stream=stream, bias=shared)
+
+    def overlapped():
+        pend = ep.dispatch_async(h, x_t, "bf16", True, recv_x=recv, topk_idx=idx_t, stream=stream)
+        shared_expert()
+        pend.wait(counts=False)  # worst-case capacity: no count readback needed
+        ep.combine(h, recv, wts_t, out=out, stream=stream, bias=shared)
+
+    def dispatch_only():
+        h.replan(idx_t, stream=stream)
+        ep.dispatch(h, x_t, "bf16", True, recv_x=recv, stream=stream)
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / n
+
+    n = max(5, min(50, args.steps // 4))
+    res = {"shared_expert": f"x[{w.T},{w.H}] @ [{w.H},{F}] @ [{F},{w.H}], bf16 torch matmul",
+           "steps": n, "dispatch_alone_ms": round(timed(dispatch_only, n), 4),
+           "shared_expert_alone_ms": round(timed(shared_expert, n), 4)}
+    h.set_num_sms(0)
+    res["serial_ms"] = round(timed(serial, n), 4)
+    best = None
+    res["overlapped_ms"] = {}
+    for sms in (0, 8, 16, 32, 64):
+        h.set_num_sms(sms)
+        t = timed(overlapped, n)
+        res["overlapped_ms"][str(sms)] = round(t, 4)
+        if best is None or t < best[1]:
+            best = (sms, t)
+    h.set_num_sms(0)
+    hideable = min(res["dispatch_alone_ms"], res["shared_expert_alone_ms"])
+    res["best_num_sms"] = best[0]
+    res["hidden_frac"] = round((res["serial_ms"] - best[1]) / hideable, 3) if hideable > 0 else None
+    if h.sync_status(stream) != ep.EP_OK:
+        raise RuntimeError("device status after the overlap runs")
+    h.destroy(stream)
+    return res
+
+
+def run_cta_profile(ep, w, idx_t, x_t, wts_t, y, stream, recv, recv_sc, out_dtype):
+    """One step (plan, dispatch, combine) with per-CTA profile records."""
+    import torch
+    h = ep.plan(idx_t, w.P, w.E, w.A, stream=stream)
+    h.profile_begin(1 << 21)
+    h.replan(idx_t, stream=stream)
+    ep.dispatch(h, x_t, out_dtype, True, recv_x=recv, recv_scales=recv_sc, stream=stream)
+    ep.combine(h, y, wts_t, out=torch.empty((w.T, w.H), dtype=torch.bfloat16, device=x_t.device),
+               stream=stream)
+    rec, dropped = h.profile_end(stream)
+    if h.sync_status(stream) != ep.EP_OK or dropped:
+        raise RuntimeError("profiled step failed or dropped records")
+    h.destroy(stream)
+    rows = []
+    for r in ep.summarize_profile(rec):
+        row = {k.replace("_ns", "_us"): (round(v / 1e3, 3) if "_ns" in k else v) for k, v in r.items()}
+        row["gbs"] = round(r["gbs"], 1)
+        rows.append(row)
+    return rows
 
 
 def main(argv=None):
@@ -547,6 +659,11 @@ def main(argv=None):
     ap.add_argument("--workload", default="bf16")
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--overlap", action="store_true",
+                    help="also time dispatch issued on the communication stream under an SM budget, "
+                         "overlapped with a shared-expert FFN on the compute stream")
+    ap.add_argument("--cta-profile", action="store_true",
+                    help="also run one step with per-CTA profile records and summarise them")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, reported as used
     if args.impl == "reference":

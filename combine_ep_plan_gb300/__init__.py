@@ -509,18 +509,20 @@ class Pending:
         self._results = results
         self._keep = keep
 
-    def wait(self):
-        """dispatch: (recv_x, recv_scales|None, N_exp, N_recv); combine: out."""
+    def wait(self, counts: bool = True):
+        """dispatch: (recv_x, recv_scales|None, N_exp, N_recv); combine: out.
+        counts=False skips the count readback (no host wait; N_exp and N_recv
+        are then returned as 0 unless the issue already read them)."""
         if not self._ptr:
             raise RuntimeError("pending call already waited on")
         ne, nr = ctypes.c_int64(), ctypes.c_int64()
-        want = self.kind == "dispatch"
+        want = self.kind == "dispatch" and counts
         code = _lib().ep_pending_wait(self._ptr, ctypes.byref(ne) if want else None,
                                       ctypes.byref(nr) if want else None)
         self._ptr = 0
         self._keep = None
         _check(code, "ep_pending_wait")
-        if want:
+        if self.kind == "dispatch":
             return self._results[0], self._results[1], ne.value, nr.value
         return self._results
 
@@ -611,7 +613,8 @@ def summarize_profile(records) -> list:
     in launch order: kernel, CTAs, units, payload bytes, span from the first
     CTA start to the last CTA end (ns), median and max CTA duration (ns),
     payload GB/s over the span, and for the plan the median stage offsets
-    from the launch's first start (route scan, phase 1, barrier), in ns."""
+    from the launch's first start, in ns: route scan and end of phase 1 over
+    the CTAs that scanned a tile, grid barrier passed over all CTAs."""
     import numpy as np
     r = np.asarray(records.cpu() if isinstance(records, torch.Tensor) else records).astype(np.uint64)
     if r.size == 0:
@@ -631,9 +634,13 @@ def summarize_profile(records) -> list:
                "cta_ns_median": float(np.median(t1 - t0)), "cta_ns_max": int((t1 - t0).max()),
                "gbs": nbytes / span if span > 0 else 0.0}
         if k == 1:
+            # route scan and end of phase 1 over the CTAs that scanned a tile
+            # (the others have no scan mark); the barrier over all CTAs
             base = t0.min()
-            for name, col in (("scan_ns", 2), ("phase1_ns", 3), ("barrier_ns", 4)):
-                v = r[m, col].astype(np.int64)
+            tiles = r[m, 2] > 0
+            for name, col, sel in (("scan_ns", 2, tiles), ("phase1_ns", 3, tiles),
+                                   ("barrier_ns", 4, np.ones_like(tiles))):
+                v = r[m, col].astype(np.int64)[sel]
                 v = v[v > 0]
                 row[name] = float(np.median(v - base)) if len(v) else 0.0
         out.append(row)

@@ -31,6 +31,7 @@ __device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi) {
 // plus a per-CTA record (items, payload bytes, start and end).
 template <int KMAX, int U, int MINB, bool PROF>
 __global__ void __launch_bounds__(256, MINB) ep_combine_kernel(CombineDev c) {
+  pdl_wait();
   unsigned long long t0 = 0, units = 0, bytes = 0;
   if (PROF && threadIdx.x == 0) t0 = prof_now();
   const int lane = threadIdx.x & 31;
@@ -150,9 +151,9 @@ cudaError_t launch_kp(const CombineDev& c, cudaStream_t stream, const LaunchCfg&
   long long grid = full;
   const long long cap = budget_cap(kernel, 256, 0, cfg.sm_budget);
   if (cap > 0 && grid > cap) grid = cap;
-  kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(c);
+  const cudaError_t e = launch_pdl(kernel, static_cast<unsigned>(grid), 256, stream, c);
   if (cfg.ctas) *cfg.ctas = grid;
-  return cudaGetLastError();
+  return e;
 }
 
 template <int KMAX, int U, int MINB>

@@ -46,6 +46,7 @@ __device__ __forceinline__ int64_t scale_at(const DispatchDev& a, int64_t r, int
 // kernel, plus a per-CTA record (items, payload bytes, start and end).
 template <int ROW_DIV, bool WITH_SCALES, bool PROF>
 __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
+  pdl_wait();
   unsigned long long t0 = 0, units = 0, bytes = 0;
   if (PROF && threadIdx.x == 0) t0 = prof_now();
   const int lane = threadIdx.x & 31;
@@ -165,6 +166,7 @@ constexpr int kFp8Units = EP_FP8_UNITS;
 
 template <bool PROF>
 __global__ void __launch_bounds__(256) ep_dispatch_fp8_kernel(DispatchDev a) {
+  pdl_wait();
   unsigned long long t0 = 0, units = 0, bytes = 0;
   if (PROF && threadIdx.x == 0) t0 = prof_now();
   const int lane = threadIdx.x & 31;
@@ -308,9 +310,9 @@ cudaError_t launch_items(Kernel kernel, const DispatchDev& d, int64_t chunks, cu
   long long grid = item_grid(d.T + d.max_pad, chunks);
   const long long cap = budget_cap(kernel, 256, 0, cfg.sm_budget);
   if (cap > 0 && grid > cap) grid = cap;
-  kernel<<<static_cast<unsigned>(grid), 256, 0, stream>>>(d);
+  const cudaError_t e = launch_pdl(kernel, static_cast<unsigned>(grid), 256, stream, d);
   if (cfg.ctas) *cfg.ctas = grid;
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

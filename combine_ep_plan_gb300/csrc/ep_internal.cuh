@@ -107,6 +107,41 @@ __device__ __forceinline__ void prof_cta_end(const Dev& d, unsigned kind, unsign
   }
 }
 
+// Programmatic dependent launch.  The dispatch and combine kernels are
+// launched with programmatic stream serialization, so that the launch of a
+// grid overlaps the end of the kernel before it in the stream: pdl_wait
+// blocks until that kernel has completed and its memory is visible, and
+// comes before every global memory access of the kernel.  None of the
+// kernels triggers its dependents early: early-launched CTAs that sit
+// waiting took SM slots from the tail of the running grid (measured slower).
+// The wait is a no-op in a kernel launched without the attribute.
+// EP_USE_PDL=0 builds plain launches.
+#ifndef EP_USE_PDL
+#define EP_USE_PDL 1
+#endif
+__device__ __forceinline__ void pdl_wait() {
+  if (EP_USE_PDL) asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename Dev>
+cudaError_t launch_pdl(void (*kernel)(Dev), unsigned grid, unsigned block, cudaStream_t stream, const Dev& arg) {
+  if (!EP_USE_PDL) {
+    kernel<<<grid, block, 0, stream>>>(arg);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, arg);
+}
+
 // How a launch is shaped: an SM budget (0 = the whole device), and where
 // the launcher reports the CTAs it launched (the profile record cursor).
 struct LaunchCfg {
