@@ -62,18 +62,19 @@ __device__ __forceinline__ uint32_t lanes_below(int l) { return l ? (0xffffffffu
 
 // Loads this tile's expert ids into shared memory (coalesced), checking them.
 // All of a thread's loads are issued before any is used.
+template <int KMAX>
 __device__ __forceinline__ void load_tile_ids(const PlanDev& p, int64_t t0, int* ids) {
   const int64_t base = t0 * p.K;
   const int64_t end = p.T * p.K;
-  const int n = kTile * p.K;  // <= kTile * EP_MAX_TOPK
-  long long v[EP_MAX_TOPK];
+  const int n = kTile * p.K;  // <= kTile * KMAX
+  long long v[KMAX];
 #pragma unroll
-  for (int u = 0; u < EP_MAX_TOPK; ++u) {
+  for (int u = 0; u < KMAX; ++u) {
     const int i = threadIdx.x + u * kTile;
     v[u] = (i < n && base + i < end) ? p.topk_idx[base + i] : -1ll;
   }
 #pragma unroll
-  for (int u = 0; u < EP_MAX_TOPK; ++u) {
+  for (int u = 0; u < KMAX; ++u) {
     const int i = threadIdx.x + u * kTile;
     if (i < n) {
       int e = -1;
@@ -106,34 +107,45 @@ __device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids
 
 // Exclusive prefix of one column over all earlier tiles: walk back through
 // predecessors 32 at a time, adding aggregates until an inclusive prefix
-// is found.  A descriptor of another epoch counts as not yet published.
+// is found.  A descriptor of another epoch counts as not yet published; a
+// window with an unpublished descriptor before the first inclusive one is
+// loaded again after a pause (one batch of loads per attempt keeps the code
+// small: this runs once per column, cold in the instruction cache).
 __device__ int lookback(const PlanDev& p, int tile, int col, bool* timed_out) {
   constexpr int kWindow = 32;
   int sum = 0;
   int j = tile - 1;
   long long polls = 0;
+  unsigned ns = 32;
   while (j >= 0) {
     unsigned long long v[kWindow];
 #pragma unroll
     for (int u = 0; u < kWindow; ++u)
       v[u] = (j - u >= 0) ? ld_desc(&p.desc[static_cast<int64_t>(j - u) * p.ncols + col]) : 0ull;
+    int part = 0;
+    bool ready = true, inclusive = false;
 #pragma unroll
     for (int u = 0; u < kWindow; ++u) {
-      if (j - u < 0) break;
-      unsigned long long d = v[u];
-      unsigned ns = 32;
-      while (static_cast<unsigned>(d >> 34) != p.epoch || ((d >> 32) & 3ull) == 0ull) {
-        if (++polls > p.poll_limit) {
-          *timed_out = true;
-          return sum;  // give up; the plan is flagged invalid
-        }
-        __nanosleep(ns);
-        if (ns < 256) ns <<= 1;
-        d = ld_desc(&p.desc[static_cast<int64_t>(j - u) * p.ncols + col]);
+      if (j - u < 0 || inclusive || !ready) continue;
+      const unsigned long long d = v[u];
+      if (static_cast<unsigned>(d >> 34) != p.epoch || ((d >> 32) & 3ull) == 0ull) {
+        ready = false;
+      } else {
+        part += static_cast<int>(static_cast<unsigned>(d));
+        inclusive = ((d >> 32) & 3ull) == kDescInclusive;
       }
-      sum += static_cast<int>(static_cast<unsigned>(d));
-      if (((d >> 32) & 3ull) == kDescInclusive) return sum;
     }
+    if (!ready) {
+      if (++polls > p.poll_limit) {
+        *timed_out = true;
+        return sum;  // give up; the plan is flagged invalid
+      }
+      __nanosleep(ns);
+      if (ns < 256) ns <<= 1;
+      continue;  // the same window again
+    }
+    sum += part;
+    if (inclusive) return sum;
     j -= kWindow;
   }
   return sum;
@@ -152,9 +164,11 @@ __device__ bool grid_sync(const PlanDev& p) {
     const unsigned arrived = atomicAdd(count, 1u) + 1u;
     int ok = 1;
     if (arrived == gridDim.x) {
-      atomicExch(count, 0u);
+      // release the waiters first; the count is reset for the next plan,
+      // which runs after this grid has ended
       __threadfence();
       atomicAdd(gen, 1u);
+      atomicExch(count, 0u);
     } else {
       long long polls = 0;
       unsigned ns = 32;
@@ -275,7 +289,7 @@ __device__ void offsets_warp_scan(const PlanDev& p, int* exp_off, int* pad_off, 
 // PROF: the same kernel, plus a per-CTA record: marks after the route scan
 // of its last tile, at the end of phase 1 and past the grid barrier; the
 // tokens it scanned.
-template <bool PROF>
+template <bool PROF, int KMAX>
 __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   extern __shared__ __align__(16) uint32_t smem[];
   unsigned long long t_start = 0, t_scan = 0, t_phase1 = 0, t_barrier = 0, scanned = 0;
@@ -288,7 +302,7 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
     const int64_t t0 = static_cast<int64_t>(tile) * kTile;
     for (int i = threadIdx.x; i < kTileWords * p.ncols; i += blockDim.x) bits[i] = 0u;
-    load_tile_ids(p, t0, ids);
+    load_tile_ids<KMAX>(p, t0, ids);
     __syncthreads();
     build_tile_bits(p, ids, bits);
     __syncthreads();
@@ -360,19 +374,19 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   // slot and exp_src, one token per thread: the token's K ids, then all
   // their window positions, are loaded before any is used.
   for (int64_t g = gtid; g < p.T; g += nthr) {
-    int e[EP_MAX_TOPK];
+    int e[KMAX];
 #pragma unroll
-    for (int k = 0; k < EP_MAX_TOPK; ++k) {
+    for (int k = 0; k < KMAX; ++k) {
       const long long v = k < p.K ? p.topk_idx[g * p.K + k] : -1ll;
       e[k] = (v >= 0 && v < p.E) ? static_cast<int>(v) : -1;
     }
     const int64_t t = g / kTile;
     const int gl = static_cast<int>(g - t * kTile);
     const int64_t word = (t * kTileWords + (gl >> 5)) * p.ncols + p.P;
-    int pre[EP_MAX_TOPK];
-    uint32_t bw[EP_MAX_TOPK];
+    int pre[KMAX];
+    uint32_t bw[KMAX];
 #pragma unroll
-    for (int k = 0; k < EP_MAX_TOPK; ++k) {
+    for (int k = 0; k < KMAX; ++k) {
       pre[k] = 0;
       bw[k] = 0u;
       if (e[k] >= 0) {
@@ -382,7 +396,7 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
     }
     const uint32_t below = lanes_below(gl & 31);
 #pragma unroll
-    for (int k = 0; k < EP_MAX_TOPK; ++k) {
+    for (int k = 0; k < KMAX; ++k) {
       if (k >= p.K) break;
       int r = -1;
       if (e[k] >= 0) {
@@ -490,14 +504,14 @@ namespace {
 // under an SM budget, two per budgeted SM), and no more than the plan's work
 // needs: one CTA per tile at least, and about one CTA per 1024 phase-2
 // outputs.  Phase 1 loops over the tiles when the grid is smaller.
-template <bool PROF>
+template <bool PROF, int KMAX>
 int plan_grid(const PlanDev& p, int sm_budget) {
   const size_t smem = plan_smem_bytes(p.P, p.E, p.K);
   static size_t cached_smem = ~static_cast<size_t>(0);
   static int cached_per_sm = 0;
   if (smem != cached_smem) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_plan_kernel<PROF>, kTile, smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_plan_kernel<PROF, KMAX>, kTile, smem) != cudaSuccess ||
         per_sm < 1)
       return 0;
     cached_per_sm = per_sm > 2 ? 2 : per_sm;
@@ -512,27 +526,33 @@ int plan_grid(const PlanDev& p, int sm_budget) {
   return static_cast<int>(grid);
 }
 
-template <bool PROF>
+template <bool PROF, int KMAX>
 cudaError_t launch_plan_t(const PlanDev& p, cudaStream_t stream, const LaunchCfg& cfg) {
   const size_t smem = plan_smem_bytes(p.P, p.E, p.K);
   if (smem > 48 * 1024) {
-    cudaError_t err = cudaFuncSetAttribute(ep_plan_kernel<PROF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t err = cudaFuncSetAttribute(ep_plan_kernel<PROF, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
   }
-  const int grid = plan_grid<PROF>(p, cfg.sm_budget);
+  const int grid = plan_grid<PROF, KMAX>(p, cfg.sm_budget);
   if (grid < 1) return cudaErrorInvalidConfiguration;
   PlanDev arg = p;
   void* args[] = {&arg};
   if (cfg.ctas) *cfg.ctas = grid;
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(ep_plan_kernel<PROF>), dim3(grid), dim3(kTile),
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(ep_plan_kernel<PROF, KMAX>), dim3(grid), dim3(kTile),
                                      args, smem, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_plan(const PlanDev& p, cudaStream_t stream, const LaunchCfg& cfg) {
-  return p.prof_rec ? launch_plan_t<true>(p, stream, cfg) : launch_plan_t<false>(p, stream, cfg);
+  // top-k arrays sized for K <= 8 or K <= 16: less unrolled code for the
+  // common small K (the kernel runs once per plan, its code cold in the
+  // instruction cache)
+  if (p.K <= 8)
+    return p.prof_rec ? launch_plan_t<true, 8>(p, stream, cfg) : launch_plan_t<false, 8>(p, stream, cfg);
+  return p.prof_rec ? launch_plan_t<true, EP_MAX_TOPK>(p, stream, cfg)
+                    : launch_plan_t<false, EP_MAX_TOPK>(p, stream, cfg);
 }
 
 }  // namespace ep

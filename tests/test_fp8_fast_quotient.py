@@ -1,9 +1,11 @@
-"""The FP8 dispatch kernel divides by the group scale with one multiply and
-two fused multiply-adds (Markstein's correction with the correctly rounded
-reciprocal) instead of a full IEEE division.  This checks, on the CPU with
-IEEE fmaf, that the E4M3 code it produces equals the code of the IEEE
-quotient for every bf16 x and bf16 amax >= 2^-60 with |x| <= amax (every
-fourth amax here; the stride-1 run covers ~1e9 pairs)."""
+"""The FP8 dispatch kernel computes the group scale amax/448 and divides by
+it with one multiply and two fused multiply-adds each (Markstein's
+correction with the correctly rounded reciprocal) instead of a full IEEE
+division.  This checks, on the CPU with IEEE fmaf, that the scale equals the
+IEEE quotient for every finite bf16 amax, and that the E4M3 code of each
+quotient equals the code of the IEEE quotient for every bf16 x and bf16
+amax >= 2^-60 with |x| <= amax (every fourth amax here; the stride-1 run
+covers ~1e9 pairs)."""
 import os
 import subprocess
 
@@ -23,5 +25,6 @@ def test_fast_quotient_gives_ieee_e4m3_codes(tmp_path, stride):
                    check=True, capture_output=True)
     r = subprocess.run([str(exe), str(stride)], capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
-    pairs, bad = r.stdout.split()[1], r.stdout.split()[3]
-    assert int(bad) == 0 and int(pairs) > 2e8
+    words = r.stdout.split()
+    pairs, bad, scale_bad = words[1], words[3], words[5]
+    assert int(bad) == 0 and int(scale_bad) == 0 and int(pairs) > 2e8
