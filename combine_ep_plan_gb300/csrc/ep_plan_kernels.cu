@@ -16,7 +16,9 @@
 //     memory; the last tile writes the column totals.
 // One bounded grid barrier.
 // Phase 2, all CTAs: with X_col(g) = #{g' < g with the bit set in column col}
-// available for any g from two loads, every plan array is computed directly:
+// available for any g from two loads (or, for the tokens of the tile a CTA
+// scanned, from the bit matrix still in its shared memory), every plan
+// array is computed directly:
 //   send_head[g][d] = X_d(g) (if routed), recv_src_idx, slot[g][k] =
 //   expert_offset[e] + X_e(g), exp_src, padding rows,
 //   recv_channel_prefix[d][s][c] = X_d(start of channel c of source s),
@@ -188,6 +190,15 @@ __device__ bool grid_sync(const PlanDev& p) {
   return s_ok != 0;
 }
 
+// Position of token i of the CTA's own tile in column col: the tile's
+// exclusive prefix plus the bits set before i in the shared bit matrix.
+__device__ __forceinline__ int tile_pos(const uint32_t* bits, const int* s_run, int ncols, int col, int i) {
+  const int w = i >> 5;
+  int pos = s_run[col];
+  for (int v = 0; v < w; ++v) pos += __popc(bits[v * ncols + col]);
+  return pos + __popc(bits[w * ncols + col] & lanes_below(i & 31));
+}
+
 // X_col(g): bits set in column col for tokens before g (g in [0, T]).
 __device__ __forceinline__ int x_at(const PlanDev& p, int col, int64_t g) {
   if (g >= p.T) return __ldcg(&p.totals[col]);
@@ -298,6 +309,7 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   // ---------------- phase 1: tiles ----------------
   uint32_t* bits = smem;                                           // [kTileWords * ncols]
   int* ids = reinterpret_cast<int*>(bits + kTileWords * p.ncols);  // [kTile * K]
+  int* s_run = ids + kTile * p.K;                                  // [ncols] tile's exclusive prefix
   bool timed_out = false;
   for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
     const int64_t t0 = static_cast<int64_t>(tile) * kTile;
@@ -325,6 +337,7 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
     }
     for (int col = threadIdx.x; col < p.ncols; col += blockDim.x) {
       int run = tile > 0 ? lookback(p, tile, col, &timed_out) : 0;
+      s_run[col] = run;
       int n = 0;
 #pragma unroll
       for (int j = 0; j < kTileWords; ++j) {
@@ -334,7 +347,7 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
       if (publish && tile > 0) st_desc(&my_desc[col], pack_desc(p.epoch, kDescInclusive, run + n));
       if (tile == p.num_tiles - 1) p.totals[col] = run + n;
     }
-    __syncthreads();  // before the next tile reuses shared memory
+    __syncthreads();  // before the next tile reuses shared memory (and for phase 2)
   }
   if (timed_out) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
   if (PROF && threadIdx.x == 0) t_phase1 = prof_now();
@@ -346,7 +359,7 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   if (PROF && threadIdx.x == 0) t_barrier = prof_now();
 
   // ---------------- phase 2: every plan array, all CTAs ----------------
-  int* exp_off = reinterpret_cast<int*>(smem);  // [E+1]
+  int* exp_off = s_run + p.ncols;               // [E+1]
   int* pad_off = exp_off + (p.E + 1);           // [E+1]
   int* recv_off = pad_off + (p.E + 1);          // [P+1]
   __shared__ int s_sizes[3];
@@ -370,40 +383,71 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
 
   const int64_t gtid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  // With at least one CTA per tile, every CTA still holds its own tile in
+  // shared memory (ids, bit matrix, exclusive prefix): its tokens' slots
+  // need no global loads.  CTAs without a tile take the small passes.  (The
+  // tile's [T,P] rows from shared memory too measured slower: the rows are
+  // better spread over all CTAs.)
+  const bool own_tile = gridDim.x >= static_cast<unsigned>(p.num_tiles);
+  const bool has_tile = own_tile && blockIdx.x < static_cast<unsigned>(p.num_tiles);
+  const int64_t extra = own_tile ? static_cast<int64_t>(gridDim.x - p.num_tiles) * blockDim.x : 0;
+  // thread range of the small passes (negative: this thread takes none)
+  const int64_t stid = extra > 0 ? gtid - static_cast<int64_t>(p.num_tiles) * blockDim.x : gtid;
+  const int64_t snthr = extra > 0 ? extra : nthr;
+  const bool small_passes = stid >= 0;
 
-  // slot and exp_src, one token per thread: the token's K ids, then all
-  // their window positions, are loaded before any is used.
-  for (int64_t g = gtid; g < p.T; g += nthr) {
-    int e[KMAX];
-#pragma unroll
-    for (int k = 0; k < KMAX; ++k) {
-      const long long v = k < p.K ? p.topk_idx[g * p.K + k] : -1ll;
-      e[k] = (v >= 0 && v < p.E) ? static_cast<int>(v) : -1;
-    }
-    const int64_t t = g / kTile;
-    const int gl = static_cast<int>(g - t * kTile);
-    const int64_t word = (t * kTileWords + (gl >> 5)) * p.ncols + p.P;
-    int pre[KMAX];
-    uint32_t bw[KMAX];
-#pragma unroll
-    for (int k = 0; k < KMAX; ++k) {
-      pre[k] = 0;
-      bw[k] = 0u;
-      if (e[k] >= 0) {
-        pre[k] = __ldcg(&p.tile_wpre[word + e[k]]);
-        bw[k] = __ldcg(&p.tile_bits[word + e[k]]);
+  if (own_tile) {
+    if (has_tile) {
+      const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTile;
+      const int i = threadIdx.x;
+      const int64_t g = t0 + i;
+      if (g < p.T) {
+        for (int k = 0; k < p.K; ++k) {
+          const int e = ids[i * p.K + k];
+          int r = -1;
+          if (e >= 0) {
+            r = exp_off[e] + tile_pos(bits, s_run, p.ncols, p.P + e, i);
+            p.exp_src[r] = static_cast<int>(g);
+          }
+          p.slot[g * p.K + k] = r;
+        }
       }
     }
-    const uint32_t below = lanes_below(gl & 31);
+  } else {
+    // slot and exp_src, one token per thread: the token's K ids, then all
+    // their window positions, are loaded before any is used.
+    for (int64_t g = gtid; g < p.T; g += nthr) {
+      int e[KMAX];
 #pragma unroll
-    for (int k = 0; k < KMAX; ++k) {
-      if (k >= p.K) break;
-      int r = -1;
-      if (e[k] >= 0) {
-        r = exp_off[e[k]] + pre[k] + __popc(bw[k] & below);
-        p.exp_src[r] = static_cast<int>(g);
+      for (int k = 0; k < KMAX; ++k) {
+        const long long v = k < p.K ? p.topk_idx[g * p.K + k] : -1ll;
+        e[k] = (v >= 0 && v < p.E) ? static_cast<int>(v) : -1;
       }
-      p.slot[g * p.K + k] = r;
+      const int64_t t = g / kTile;
+      const int gl = static_cast<int>(g - t * kTile);
+      const int64_t word = (t * kTileWords + (gl >> 5)) * p.ncols + p.P;
+      int pre[KMAX];
+      uint32_t bw[KMAX];
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        pre[k] = 0;
+        bw[k] = 0u;
+        if (e[k] >= 0) {
+          pre[k] = __ldcg(&p.tile_wpre[word + e[k]]);
+          bw[k] = __ldcg(&p.tile_bits[word + e[k]]);
+        }
+      }
+      const uint32_t below = lanes_below(gl & 31);
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k) {
+        if (k >= p.K) break;
+        int r = -1;
+        if (e[k] >= 0) {
+          r = exp_off[e[k]] + pre[k] + __popc(bw[k] & below);
+          p.exp_src[r] = static_cast<int>(g);
+        }
+        p.slot[g * p.K + k] = r;
+      }
     }
   }
 
@@ -449,7 +493,8 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
 #pragma unroll 2
   // The small passes below start at different points of the thread range,
   // so that they do not all land on the first CTAs after the slot pass.
-  for (int64_t i = (gtid + nthr / 2) % nthr; i < static_cast<int64_t>(p.P) * p.P * p.C; i += nthr) {
+  for (int64_t i = small_passes ? (stid + snthr / 2) % snthr : INT64_MAX; i < static_cast<int64_t>(p.P) * p.P * p.C;
+       i += snthr) {
     const int c = static_cast<int>(i % p.C);
     const int64_t sd = i / p.C;
     const int d = static_cast<int>(sd % p.P);
@@ -468,14 +513,15 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   }
 
   // per-source expert counts
-  for (int i = static_cast<int>((gtid + 3 * nthr / 4) % nthr); i < p.P * p.E; i += static_cast<int>(nthr)) {
+  for (int i = small_passes ? static_cast<int>((stid + 3 * snthr / 4) % snthr) : INT32_MAX; i < p.P * p.E;
+       i += static_cast<int>(snthr)) {
     const int s = i / p.E;
     const int e = i - s * p.E;
     p.ntpe[i] = x_at(p, p.P + e, (s + 1) * p.S) - x_at(p, p.P + e, static_cast<int64_t>(s) * p.S);
   }
 
   // padding rows of the expanded layout
-  for (int64_t i = (gtid + nthr / 4) % nthr; i < n_pad; i += nthr) {
+  for (int64_t i = small_passes ? (stid + snthr / 4) % snthr : INT64_MAX; i < n_pad; i += snthr) {
     int lo = 0, hi = p.E;  // e with pad_off[e] <= i < pad_off[e+1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -493,17 +539,23 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
 }  // namespace
 
 size_t plan_smem_bytes(int P, int E, int K) {
-  const size_t phase1 = sizeof(uint32_t) * kTileWords * (P + E) + sizeof(int) * kTile * K;
-  const size_t phase2 = sizeof(int) * (2 * (E + 1) + (P + 1));
-  return phase1 > phase2 ? phase1 : phase2;
+  // phase 1: bit matrix, ids, exclusive prefix per column (kept for phase 2);
+  // phase 2: the offsets
+  return sizeof(uint32_t) * kTileWords * (P + E) + sizeof(int) * (kTile * K + (P + E)) +
+         sizeof(int) * (2 * (E + 1) + (P + 1));
 }
+
+// Phase-2 outputs per CTA that size the grid (tuning knob).
+#ifndef EP_PLAN_WORK_PER_CTA
+#define EP_PLAN_WORK_PER_CTA 1024
+#endif
 
 namespace {
 
 // Co-resident CTAs (at most two per SM, which keeps the grid barrier cheap;
 // under an SM budget, two per budgeted SM), and no more than the plan's work
-// needs: one CTA per tile at least, and about one CTA per 1024 phase-2
-// outputs.  Phase 1 loops over the tiles when the grid is smaller.
+// needs: one CTA per tile at least, and about one CTA per
+// EP_PLAN_WORK_PER_CTA phase-2 outputs.  Phase 1 loops over the tiles when the grid is smaller.
 template <bool PROF, int KMAX>
 int plan_grid(const PlanDev& p, int sm_budget) {
   const size_t smem = plan_smem_bytes(p.P, p.E, p.K);
@@ -520,7 +572,7 @@ int plan_grid(const PlanDev& p, int sm_budget) {
   const int sms = sm_budget > 0 && sm_budget < num_sms() ? sm_budget : num_sms();
   const int64_t cap = static_cast<int64_t>(cached_per_sm) * sms;
   const int64_t work = p.T * (p.K + p.P) + static_cast<int64_t>(p.P) * p.P * p.C + static_cast<int64_t>(p.P) * p.E;
-  int64_t grid = (work + 1023) / 1024;
+  int64_t grid = (work + EP_PLAN_WORK_PER_CTA - 1) / EP_PLAN_WORK_PER_CTA;
   if (grid < p.num_tiles) grid = p.num_tiles;
   if (grid > cap) grid = cap;
   return static_cast<int>(grid);

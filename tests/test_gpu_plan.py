@@ -87,6 +87,16 @@ def test_plan_one_expert_per_rank_many_tiles():
     assert_plan_equal(gpu, oracle.plan(idx, w.S, w.P, w.E, w.A))
 
 
+def test_plan_more_tiles_than_resident_ctas():
+    """375 tiles: more than the co-resident grid, so CTAs loop over tiles in
+    phase 1 and phase 2 takes every position from global memory."""
+    w = WORKLOADS["tiny"].scaled(P=8, E=16, S=12000, K=2, A=4)
+    idx, _ = draw_topk(w)
+    idx[::7, 1] = -1
+    h, gpu = _run(w, idx, 5)
+    assert_plan_equal(gpu, oracle.plan(idx, w.S, w.P, w.E, w.A, 5))
+
+
 def test_replan_reuses_handle():
     w = WORKLOADS["bf16"].scaled(S=257)
     idx0, _ = draw_topk(w, seed=3)
