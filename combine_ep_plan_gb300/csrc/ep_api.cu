@@ -49,6 +49,7 @@ struct ep_handle_s {
   int64_t cap_recv = 0, cap_exp = 0, cap_pad = 0;
   int device = 0;
   unsigned epoch = 0;
+  unsigned bar_count = 0;  // grid-barrier arrivals of this handle's plans so far
   // SM budget of the dispatch, combine and backward launches (0 = all)
   int sm_budget = 0;
   // asynchronous calls: communication stream, pinned count slots in use,
@@ -226,9 +227,12 @@ ep_status_t enqueue_plan(ep_handle_s* h, const int64_t* topk_idx, cudaStream_t s
   h->epoch = (h->epoch + 1u) & 0x3fffffffu;
   if (h->epoch == 0u) h->epoch = 1u;  // epoch 0 is what cleared memory holds
   h->dev.epoch = h->epoch;
+  h->dev.bar_base = h->bar_count;
   Launch L(h);
   L.target(h->dev);
-  return cuda_status(finish_launch(h, L, ep::launch_plan(h->dev, stream, L.cfg)));
+  const cudaError_t e = ep::launch_plan(h->dev, stream, L.cfg);
+  if (e == cudaSuccess) h->bar_count += static_cast<unsigned>(L.ctas);
+  return cuda_status(finish_launch(h, L, e));
 }
 
 ep_status_t read_status_word(ep_handle_s* h, cudaStream_t stream, bool clear, int sizes[3]) {
@@ -242,11 +246,14 @@ ep_status_t read_status_word(ep_handle_s* h, cudaStream_t stream, bool clear, in
     if (e != cudaSuccess) return cuda_status(e);
   }
   if (clear && st) {
-    // after a timed-out wait the grid-barrier words may be off: reset them too
+    // after a timed-out wait the barrier count may be short: reset it too
     const unsigned zeros[ep::kCtrWords] = {};
-    e = (st & ep::kStTimeout)
-            ? cudaMemcpy(h->dev.ctr, zeros, sizeof zeros, cudaMemcpyHostToDevice)
-            : cudaMemcpy(h->dev.ctr + ep::kCtrStatus, zeros, sizeof(unsigned), cudaMemcpyHostToDevice);
+    if (st & ep::kStTimeout) {
+      e = cudaMemcpy(h->dev.ctr, zeros, sizeof zeros, cudaMemcpyHostToDevice);
+      h->bar_count = 0;
+    } else {
+      e = cudaMemcpy(h->dev.ctr + ep::kCtrStatus, zeros, sizeof(unsigned), cudaMemcpyHostToDevice);
+    }
     if (e != cudaSuccess) return cuda_status(e);
   }
   if (st & (ep::kStInvalidId | ep::kStDuplicate)) return EP_ERR_INVALID;

@@ -18,12 +18,12 @@ constexpr unsigned kStCapacity = 4u;    // an output row at or beyond capacity
 constexpr unsigned kStTimeout = 8u;     // bounded look-back wait gave up
 
 // Control words (zeroed when a handle is created), each in its own 128-byte
-// line: the barrier's waiters poll the generation word while arrivals
-// update the count.
-constexpr int kCtrBarCount = 0;   // grid barrier: CTAs arrived
-constexpr int kCtrBarGen = 32;    // grid barrier: generation
-constexpr int kCtrStatus = 64;    // device status word
-constexpr int kCtrWords = 96;
+// line.  The grid barrier's arrival count is never reset: each plan waits
+// for it to reach bar_base + its grid size, bar_base being the CTAs of the
+// handle's earlier plans (kept on the host).
+constexpr int kCtrBarCount = 0;   // grid barrier: CTAs arrived, all plans
+constexpr int kCtrStatus = 32;    // device status word
+constexpr int kCtrWords = 64;
 
 // Size slots.
 constexpr int kSizeRecv = 0;  // N_recv
@@ -187,6 +187,8 @@ struct PlanDev {
   int* exp_src;        // [T*K + E*(A-1)]
   int* pad_rows;       // [E*(A-1)]
   unsigned char* in_rank;  // [T,P]
+  // arrivals at the grid barrier before this plan (see kCtrBarCount)
+  unsigned bar_base;
   // bounded wait of the look-back, and a test hook
   long long poll_limit;
   int suppress_tile;

@@ -153,37 +153,28 @@ __device__ int lookback(const PlanDev& p, int tile, int col, bool* timed_out) {
   return sum;
 }
 
-// Bounded grid-wide barrier for a cooperative launch: the last CTA to arrive
-// resets the count and bumps the generation the others wait on.
+// Bounded grid-wide barrier for a cooperative launch.  Each CTA adds one
+// arrival (a release reduction: nothing to wait for) and polls the count
+// until it reaches this plan's target: the release of the last CTA is the
+// one reduction, seen by each poller one load later.
 __device__ bool grid_sync(const PlanDev& p) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     unsigned* count = p.ctr + kCtrBarCount;
-    unsigned* gen = p.ctr + kCtrBarGen;
-    const unsigned g0 = ld_acquire(gen);
-    __threadfence();
-    const unsigned arrived = atomicAdd(count, 1u) + 1u;
+    const unsigned target = p.bar_base + gridDim.x;
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
     int ok = 1;
-    if (arrived == gridDim.x) {
-      // release the waiters first; the count is reset for the next plan,
-      // which runs after this grid has ended
-      __threadfence();
-      atomicAdd(gen, 1u);
-      atomicExch(count, 0u);
-    } else {
-      long long polls = 0;
-      unsigned ns = 32;
-      while (ld_acquire(gen) == g0) {
-        if (++polls > p.poll_limit) {
-          ok = 0;
-          break;
-        }
-        __nanosleep(ns);
-        if (ns < 128) ns <<= 1;
+    long long polls = 0;
+    unsigned ns = 32;
+    while (static_cast<int>(ld_acquire(count) - target) < 0) {
+      if (++polls > p.poll_limit) {
+        ok = 0;
+        break;
       }
+      __nanosleep(ns);
+      if (ns < 128) ns <<= 1;
     }
-    __threadfence();
     s_ok = ok;
   }
   __syncthreads();
@@ -362,6 +353,7 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   int* exp_off = s_run + p.ncols;               // [E+1]
   int* pad_off = exp_off + (p.E + 1);           // [E+1]
   int* recv_off = pad_off + (p.E + 1);          // [P+1]
+  int* s_slot = recv_off + (p.P + 1);           // [kTile * K] own tile's slots
   __shared__ int s_sizes[3];
   if (threadIdx.x < 32) offsets_warp_scan(p, exp_off, pad_off, recv_off, s_sizes);
   __syncthreads();
@@ -398,20 +390,24 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
 
   if (own_tile) {
     if (has_tile) {
+      // one token per thread; the slots are staged in shared memory and
+      // leave as one contiguous block
       const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kTile;
+      const int n_tok = static_cast<int>(min64(kTile, p.T - t0));
       const int i = threadIdx.x;
-      const int64_t g = t0 + i;
-      if (g < p.T) {
+      if (i < n_tok) {
         for (int k = 0; k < p.K; ++k) {
           const int e = ids[i * p.K + k];
           int r = -1;
           if (e >= 0) {
             r = exp_off[e] + tile_pos(bits, s_run, p.ncols, p.P + e, i);
-            p.exp_src[r] = static_cast<int>(g);
+            p.exp_src[r] = static_cast<int>(t0 + i);
           }
-          p.slot[g * p.K + k] = r;
+          s_slot[i * p.K + k] = r;
         }
       }
+      __syncthreads();
+      for (int j = threadIdx.x; j < n_tok * p.K; j += blockDim.x) p.slot[t0 * p.K + j] = s_slot[j];
     }
   } else {
     // slot and exp_src, one token per thread: the token's K ids, then all
@@ -460,15 +456,18 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   {
     const int64_t words = (p.T + 31) / 32;
     const int64_t lanes_d = (nthr / p.P) * p.P;  // threads used: a multiple of P
+    // the largest split that still gives every thread at most one unit
     int sub = 1;
-    while (sub < 32 && words * sub * p.P < lanes_d) sub <<= 1;
+    while (sub < 32 && words * (2 * sub) * p.P <= lanes_d) sub <<= 1;
     const int per = 32 / sub;
     const int log_sub = __ffs(sub) - 1;
-    if (gtid < lanes_d) {
-      const int d = static_cast<int>(gtid % p.P);
+    // units go to the CTAs without a tile first: the others have slots to write
+    const int64_t dtid = own_tile ? (gtid + nthr - static_cast<int64_t>(p.num_tiles) * blockDim.x) % nthr : gtid;
+    if (dtid < lanes_d) {
+      const int d = static_cast<int>(dtid % p.P);
       const int base = recv_off[d];
       const int64_t step = lanes_d / p.P;
-      for (int64_t wq = gtid / p.P; wq < words * sub; wq += step) {
+      for (int64_t wq = dtid / p.P; wq < words * sub; wq += step) {
         const int64_t tw = wq >> log_sub;  // word index: tile * kTileWords + warp
         const int l0 = static_cast<int>(wq & (sub - 1)) * per;
         const int64_t at = tw * p.ncols + d;
@@ -540,9 +539,9 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
 
 size_t plan_smem_bytes(int P, int E, int K) {
   // phase 1: bit matrix, ids, exclusive prefix per column (kept for phase 2);
-  // phase 2: the offsets
+  // phase 2: the offsets and the own tile's slots
   return sizeof(uint32_t) * kTileWords * (P + E) + sizeof(int) * (kTile * K + (P + E)) +
-         sizeof(int) * (2 * (E + 1) + (P + 1));
+         sizeof(int) * (2 * (E + 1) + (P + 1) + kTile * K);
 }
 
 // Phase-2 outputs per CTA that size the grid (tuning knob).
