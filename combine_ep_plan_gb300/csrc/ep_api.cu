@@ -8,6 +8,7 @@
 // descriptors are cleared, once, when the handle is made: each plan tags its
 // descriptors with a new epoch, and every other array is fully written by
 // each plan.
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -77,16 +78,15 @@ struct ep_pending_s {
 namespace ep {
 
 int num_sms() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];  // zero-initialised (static storage)
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-    cached[dev] = n;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev].store(n, std::memory_order_relaxed);
   }
-  return cached[dev];
+  return n;
 }
 
 }  // namespace ep

@@ -144,7 +144,7 @@ int resident_grid(Kernel kernel, int threads) {
 
 template <int KMAX, int U, int MINB, bool PROF>
 cudaError_t launch_kp(const CombineDev& c, cudaStream_t stream, const LaunchCfg& cfg) {
-  static int full = 0;  // per process; one device type
+  thread_local int full = 0;  // per host thread; one device type per process
   auto kernel = ep_combine_kernel<KMAX, U, MINB, PROF>;
   if (full == 0)
     full = EP_COMBINE_CTAS_PER_SM > 0 ? EP_COMBINE_CTAS_PER_SM * num_sms() : resident_grid(kernel, 256);

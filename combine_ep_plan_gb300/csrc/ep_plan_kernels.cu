@@ -558,8 +558,9 @@ namespace {
 template <bool PROF, int KMAX>
 int plan_grid(const PlanDev& p, int sm_budget) {
   const size_t smem = plan_smem_bytes(p.P, p.E, p.K);
-  static size_t cached_smem = ~static_cast<size_t>(0);
-  static int cached_per_sm = 0;
+  // occupancy per host thread (one device type per process)
+  thread_local size_t cached_smem = ~static_cast<size_t>(0);
+  thread_local int cached_per_sm = 0;
   if (smem != cached_smem) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_plan_kernel<PROF, KMAX>, kTile, smem) != cudaSuccess ||
