@@ -20,7 +20,7 @@ import torch
 
 __all__ = [
     "EPError", "EPHandle", "plan", "dispatch", "dispatch_fresh", "dispatch_cached", "combine",
-    "worst_expanded_rows", "library_path", "load_library", "FIELDS", "set_lookback_debug",
+    "worst_expanded_rows", "library_path", "load_library", "FIELDS", "set_plan_wait_debug",
     "dispatch_backward", "combine_backward", "dispatch_metadata",
     "Pending", "dispatch_async", "combine_async", "PROFILE_KERNELS", "PROFILE_WORDS", "summarize_profile",
 ]
@@ -116,8 +116,8 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
     lib.ep_handle_info.argtypes = [vp, ctypes.POINTER(i64)] + [ctypes.POINTER(i32)] * 5
     lib.ep_handle_destroy.restype = st
     lib.ep_handle_destroy.argtypes = [vp, vp]
-    lib.ep_debug_set_lookback.restype = None
-    lib.ep_debug_set_lookback.argtypes = [i64, i32]
+    lib.ep_debug_set_plan_wait.restype = None
+    lib.ep_debug_set_plan_wait.argtypes = [i64, i32]
     lib.ep_set_num_sms.restype = st
     lib.ep_set_num_sms.argtypes = [vp, i32]
     lib.ep_dispatch_async.restype = st
@@ -647,6 +647,6 @@ def summarize_profile(records) -> list:
     return out
 
 
-def set_lookback_debug(poll_limit: int = 0, suppress_tile: int = -1):
-    """Test hook for the plan scan's bounded wait (see ep_debug_set_lookback)."""
-    _lib().ep_debug_set_lookback(poll_limit, suppress_tile)
+def set_plan_wait_debug(poll_limit: int = 0, suppress_tile: int = -1):
+    """Test hook for the plan's bounded grid-barrier waits (see ep_debug_set_plan_wait)."""
+    _lib().ep_debug_set_plan_wait(poll_limit, suppress_tile)

@@ -4,10 +4,9 @@
 // A handle owns one stream-ordered device allocation carved by a cursor into
 // regions (the symmetric-workspace idea of "Ascend DeepEP MoE Dispatch
 // Optimization", section "Workspace 不是一个 Tensor，而是一块地址空间", here a
-// single-device window).  Only the control words and the look-back
-// descriptors are cleared, once, when the handle is made: each plan tags its
-// descriptors with a new epoch, and every other array is fully written by
-// each plan.
+// single-device window).  Only the control words are cleared, once, when
+// the handle is made; every other array is fully written by each plan
+// before it is read.
 #include <atomic>
 #include <climits>
 #include <cstdint>
@@ -20,7 +19,7 @@
 
 namespace {
 
-constexpr int kAbiVersion = 3;
+constexpr int kAbiVersion = 4;
 constexpr long long kDefaultPollLimit = 1ll << 20;
 
 long long g_poll_limit = kDefaultPollLimit;
@@ -49,7 +48,6 @@ struct ep_handle_s {
   size_t zero_bytes = 0;
   int64_t cap_recv = 0, cap_exp = 0, cap_pad = 0;
   int device = 0;
-  unsigned epoch = 0;
   unsigned bar_count = 0;  // grid-barrier arrivals of this handle's plans so far
   // SM budget of the dispatch, combine and backward launches (0 = all)
   int sm_budget = 0;
@@ -166,12 +164,11 @@ size_t layout_handle(ep_handle_s* h, char* base) {
   ep::PlanDev& p = h->dev;
   const int64_t T = p.T, P = p.P, E = p.E, K = p.K, C = p.C, A = p.A;
   Layout L;
-  // control words and look-back descriptors (cleared once per handle: the
-  // pool may hand back memory that holds another handle's descriptors with
-  // the same epoch numbers), then scratch
+  // control words (cleared once per handle), then scratch
   const size_t o_ctr = L.take(sizeof(unsigned) * ep::kCtrWords);
-  const size_t o_desc = L.take(sizeof(unsigned long long) * p.num_tiles * (P + E));
   h->zero_bytes = L.off;
+  const size_t o_agg = L.take(sizeof(int) * p.num_tiles * (P + E));
+  const size_t o_tpre = L.take(sizeof(int) * p.num_tiles * (P + E));
   const size_t o_bits = L.take(sizeof(uint32_t) * p.num_tiles * ep::kTileWords * (P + E));
   const size_t o_wpre = L.take(sizeof(int) * p.num_tiles * ep::kTileWords * (P + E));
   const size_t o_sizes = L.take(sizeof(int) * ep::kSizeWords);
@@ -202,7 +199,8 @@ size_t layout_handle(ep_handle_s* h, char* base) {
     p.sizes = reinterpret_cast<int*>(base + o_sizes);
     p.totals = reinterpret_cast<int*>(base + o_totals);
     p.ntpe = reinterpret_cast<int*>(base + o_ntpe);
-    p.desc = reinterpret_cast<unsigned long long*>(base + o_desc);
+    p.agg = reinterpret_cast<int*>(base + o_agg);
+    p.tile_pre = reinterpret_cast<int*>(base + o_tpre);
     p.ntpr = reinterpret_cast<int*>(base + o_ntpr);
     p.rpm = reinterpret_cast<int*>(base + o_rpm);
     p.cpm = reinterpret_cast<int*>(base + o_cpm);
@@ -224,14 +222,11 @@ ep_status_t enqueue_plan(ep_handle_s* h, const int64_t* topk_idx, cudaStream_t s
   h->dev.topk_idx = topk_idx;
   h->dev.poll_limit = g_poll_limit;
   h->dev.suppress_tile = g_suppress_tile;
-  h->epoch = (h->epoch + 1u) & 0x3fffffffu;
-  if (h->epoch == 0u) h->epoch = 1u;  // epoch 0 is what cleared memory holds
-  h->dev.epoch = h->epoch;
   h->dev.bar_base = h->bar_count;
   Launch L(h);
   L.target(h->dev);
   const cudaError_t e = ep::launch_plan(h->dev, stream, L.cfg);
-  if (e == cudaSuccess) h->bar_count += static_cast<unsigned>(L.ctas);
+  if (e == cudaSuccess) h->bar_count += 2u * static_cast<unsigned>(L.ctas);  // two barriers
   return cuda_status(finish_launch(h, L, e));
 }
 
@@ -793,7 +788,7 @@ ep_status_t ep_pending_wait(ep_pending_t p, int64_t* n_exp, int64_t* n_recv) {
   return st;
 }
 
-void ep_debug_set_lookback(int64_t poll_limit, int suppress_tile) {
+void ep_debug_set_plan_wait(int64_t poll_limit, int suppress_tile) {
   g_poll_limit = poll_limit > 0 ? poll_limit : kDefaultPollLimit;
   g_suppress_tile = suppress_tile;
 }

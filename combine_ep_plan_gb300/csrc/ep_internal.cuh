@@ -8,19 +8,22 @@
 namespace ep {
 
 // Tokens handled by one CTA of the plan kernels (one thread per token).
-constexpr int kTile = 256;
+#ifndef EP_TILE
+#define EP_TILE 256
+#endif
+constexpr int kTile = EP_TILE;
 constexpr int kTileWords = kTile / 32;
 
 // Bits of the device status word.
 constexpr unsigned kStInvalidId = 1u;   // expert id outside [-1, E)
 constexpr unsigned kStDuplicate = 2u;   // same expert twice in one token row
 constexpr unsigned kStCapacity = 4u;    // an output row at or beyond capacity
-constexpr unsigned kStTimeout = 8u;     // bounded look-back wait gave up
+constexpr unsigned kStTimeout = 8u;     // a bounded grid-barrier wait gave up
 
 // Control words (zeroed when a handle is created), each in its own 128-byte
-// line.  The grid barrier's arrival count is never reset: each plan waits
-// for it to reach bar_base + its grid size, bar_base being the CTAs of the
-// handle's earlier plans (kept on the host).
+// line.  The grid barriers' arrival count is never reset: a plan's barrier
+// r (1 or 2) waits for it to reach bar_base + r * its grid size, bar_base
+// being the arrivals of the handle's earlier plans (kept on the host).
 constexpr int kCtrBarCount = 0;   // grid barrier: CTAs arrived, all plans
 constexpr int kCtrStatus = 32;    // device status word
 constexpr int kCtrWords = 64;
@@ -149,11 +152,6 @@ struct LaunchCfg {
   long long* ctas = nullptr;
 };
 
-// Look-back descriptor: high 32 bits = (plan epoch << 2) | state, low 32
-// bits = value.
-constexpr unsigned long long kDescAggregate = 1ull;
-constexpr unsigned long long kDescInclusive = 2ull;
-
 // Everything the plan kernels need, passed by value.
 struct PlanDev {
   // shape
@@ -166,10 +164,10 @@ struct PlanDev {
   const int64_t* topk_idx;
   // scratch
   unsigned* ctr;       // [kCtrWords], zeroed once per handle
-  unsigned epoch;      // this plan's epoch (>= 1), tags the descriptors
-  unsigned long long* desc;  // [num_tiles, P+E] look-back descriptors
   uint32_t* tile_bits; // [num_tiles, kTileWords, P+E] tile bit matrices
-  int* tile_wpre;      // [num_tiles, kTileWords, P+E] exclusive prefix per word
+  int* tile_wpre;      // [num_tiles, kTileWords, P+E] exclusive prefix per word inside the tile
+  int* agg;            // [P+E, num_tiles] bits per tile and column
+  int* tile_pre;       // [P+E, num_tiles] exclusive prefix of each tile over the tiles before it
   // outputs
   int* sizes;          // [kSizeWords]
   int* totals;         // [P+E]: num_recv[d], then expert_counts[e]
@@ -187,9 +185,10 @@ struct PlanDev {
   int* exp_src;        // [T*K + E*(A-1)]
   int* pad_rows;       // [E*(A-1)]
   unsigned char* in_rank;  // [T,P]
-  // arrivals at the grid barrier before this plan (see kCtrBarCount)
+  // arrivals at the grid barriers before this plan (see kCtrBarCount)
   unsigned bar_base;
-  // bounded wait of the look-back, and a test hook
+  // bounded wait of the grid barriers, and a test hook (a tile whose CTA
+  // returns before the first barrier)
   long long poll_limit;
   int suppress_tile;
   EP_PROF_FIELDS;

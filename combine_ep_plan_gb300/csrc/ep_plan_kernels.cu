@@ -7,16 +7,15 @@
 //     slots that land on one rank), column P+e = "token picked expert e";
 //     per-lane shared-memory atomicOr; invalid and duplicate ids are
 //     reported;
-//   - a single-pass decoupled look-back over tiles, column by column: each
-//     descriptor packs (plan epoch, state, value) in one 64-bit word, so a
-//     reader needs no fence pairs and stale descriptors of an earlier plan are
-//     ignored without clearing; 32 predecessors per poll; every wait is
-//     bounded;
-//   - the tile's bit matrix and its per-word exclusive prefixes go to global
-//     memory; the last tile writes the column totals.
-// One bounded grid barrier.
+//   - the tile's bit matrix, its per-word prefixes inside the tile and its
+//     count per column go to global memory.
+// Grid barrier 1.  Column scans: one warp per column turns the tiles' counts
+// into each tile's exclusive prefix and the column total.  Grid barrier 2
+// (both barriers bounded).  (A single-pass decoupled look-back over the
+// tiles, with one barrier, measured slower: every tile reached its
+// predecessors while they were still publishing.)
 // Phase 2, all CTAs: with X_col(g) = #{g' < g with the bit set in column col}
-// available for any g from two loads (or, for the tokens of the tile a CTA
+// available for any g from three loads (or, for the tokens of the tile a CTA
 // scanned, from the bit matrix still in its shared memory), every plan
 // array is computed directly:
 //   send_head[g][d] = X_d(g) (if routed), recv_src_idx, slot[g][k] =
@@ -38,26 +37,15 @@ namespace {
 
 __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
 
-__device__ __forceinline__ unsigned long long ld_desc(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_desc(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-__device__ __forceinline__ unsigned long long pack_desc(unsigned epoch, unsigned long long state, int value) {
-  return (static_cast<unsigned long long>((epoch << 2) | static_cast<unsigned>(state)) << 32) |
-         static_cast<unsigned>(value);
-}
+// Plan threads resident per SM at most (a small grid keeps the grid
+// barriers cheap).
+constexpr int kPlanThreadsPerSm = 512;
 
 // Lanes below l within a word.
 __device__ __forceinline__ uint32_t lanes_below(int l) { return l ? (0xffffffffu >> (32 - l)) : 0u; }
@@ -107,62 +95,17 @@ __device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids
   }
 }
 
-// Exclusive prefix of one column over all earlier tiles: walk back through
-// predecessors 32 at a time, adding aggregates until an inclusive prefix
-// is found.  A descriptor of another epoch counts as not yet published; a
-// window with an unpublished descriptor before the first inclusive one is
-// loaded again after a pause (one batch of loads per attempt keeps the code
-// small: this runs once per column, cold in the instruction cache).
-__device__ int lookback(const PlanDev& p, int tile, int col, bool* timed_out) {
-  constexpr int kWindow = 32;
-  int sum = 0;
-  int j = tile - 1;
-  long long polls = 0;
-  unsigned ns = 32;
-  while (j >= 0) {
-    unsigned long long v[kWindow];
-#pragma unroll
-    for (int u = 0; u < kWindow; ++u)
-      v[u] = (j - u >= 0) ? ld_desc(&p.desc[static_cast<int64_t>(j - u) * p.ncols + col]) : 0ull;
-    int part = 0;
-    bool ready = true, inclusive = false;
-#pragma unroll
-    for (int u = 0; u < kWindow; ++u) {
-      if (j - u < 0 || inclusive || !ready) continue;
-      const unsigned long long d = v[u];
-      if (static_cast<unsigned>(d >> 34) != p.epoch || ((d >> 32) & 3ull) == 0ull) {
-        ready = false;
-      } else {
-        part += static_cast<int>(static_cast<unsigned>(d));
-        inclusive = ((d >> 32) & 3ull) == kDescInclusive;
-      }
-    }
-    if (!ready) {
-      if (++polls > p.poll_limit) {
-        *timed_out = true;
-        return sum;  // give up; the plan is flagged invalid
-      }
-      __nanosleep(ns);
-      if (ns < 256) ns <<= 1;
-      continue;  // the same window again
-    }
-    sum += part;
-    if (inclusive) return sum;
-    j -= kWindow;
-  }
-  return sum;
-}
-
 // Bounded grid-wide barrier for a cooperative launch.  Each CTA adds one
 // arrival (a release reduction: nothing to wait for) and polls the count
-// until it reaches this plan's target: the release of the last CTA is the
-// one reduction, seen by each poller one load later.
-__device__ bool grid_sync(const PlanDev& p) {
+// until it reaches this barrier's target, the arrivals of the handle's
+// earlier plans plus `round` times the grid: the release of the last CTA is
+// the one reduction, seen by each poller one load later.
+__device__ bool grid_sync(const PlanDev& p, unsigned round) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     unsigned* count = p.ctr + kCtrBarCount;
-    const unsigned target = p.bar_base + gridDim.x;
+    const unsigned target = p.bar_base + round * gridDim.x;
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
     int ok = 1;
     long long polls = 0;
@@ -181,6 +124,41 @@ __device__ bool grid_sync(const PlanDev& p) {
   return s_ok != 0;
 }
 
+// Column scans, one warp per column: the tiles' counts in order, 32 at a
+// time, to each tile's exclusive prefix (tile_pre) and the column total.
+__device__ void column_scans(const PlanDev& p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gwarp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t col = gwarp; col < p.ncols; col += nwarps) {
+    const int* agg = p.agg + col * p.num_tiles;
+    int* pre = p.tile_pre + col * p.num_tiles;
+    int carry = 0;
+    constexpr int kBatch = 8;  // chunks of 32 tiles loaded before any is scanned
+    for (int b0 = 0; b0 < p.num_tiles; b0 += 32 * kBatch) {
+      int v[kBatch];
+#pragma unroll
+      for (int c = 0; c < kBatch; ++c) {
+        const int t = b0 + 32 * c + lane;
+        v[c] = t < p.num_tiles ? __ldcg(&agg[t]) : 0;
+      }
+#pragma unroll
+      for (int c = 0; c < kBatch; ++c) {
+        const int t = b0 + 32 * c + lane;
+        int inc = v[c];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, inc, o);
+          if (lane >= o) inc += n;
+        }
+        if (t < p.num_tiles) pre[t] = carry + inc - v[c];
+        carry += __shfl_sync(0xffffffffu, inc, 31);
+      }
+    }
+    if (lane == 0) p.totals[col] = carry;
+  }
+}
+
 // Position of token i of the CTA's own tile in column col: the tile's
 // exclusive prefix plus the bits set before i in the shared bit matrix.
 __device__ __forceinline__ int tile_pos(const uint32_t* bits, const int* s_run, int ncols, int col, int i) {
@@ -196,7 +174,8 @@ __device__ __forceinline__ int x_at(const PlanDev& p, int col, int64_t g) {
   const int64_t t = g / kTile;
   const int gl = static_cast<int>(g - t * kTile);
   const int64_t at = (t * kTileWords + (gl >> 5)) * p.ncols + col;
-  return __ldcg(&p.tile_wpre[at]) + __popc(__ldcg(&p.tile_bits[at]) & lanes_below(gl & 31));
+  return __ldcg(&p.tile_pre[static_cast<int64_t>(col) * p.num_tiles + t]) + __ldcg(&p.tile_wpre[at]) +
+         __popc(__ldcg(&p.tile_bits[at]) & lanes_below(gl & 31));
 }
 
 // One warp turns the column totals into the offsets, in shared memory:
@@ -289,20 +268,20 @@ __device__ void offsets_warp_scan(const PlanDev& p, int* exp_off, int* pad_off, 
 }
 
 // PROF: the same kernel, plus a per-CTA record: marks after the route scan
-// of its last tile, at the end of phase 1 and past the grid barrier; the
-// tokens it scanned.
+// of its last tile and past each grid barrier; the tokens it scanned.
 template <bool PROF, int KMAX>
-__global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
+__global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kernel(PlanDev p) {
   extern __shared__ __align__(16) uint32_t smem[];
-  unsigned long long t_start = 0, t_scan = 0, t_phase1 = 0, t_barrier = 0, scanned = 0;
+  unsigned long long t_start = 0, t_scan = 0, t_bar1 = 0, t_bar2 = 0, scanned = 0;
   if (PROF && threadIdx.x == 0) t_start = prof_now();
 
   // ---------------- phase 1: tiles ----------------
   uint32_t* bits = smem;                                           // [kTileWords * ncols]
   int* ids = reinterpret_cast<int*>(bits + kTileWords * p.ncols);  // [kTile * K]
   int* s_run = ids + kTile * p.K;                                  // [ncols] tile's exclusive prefix
-  bool timed_out = false;
   for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    // test hook: a tile that never arrives at the first barrier
+    if (tile == p.suppress_tile) return;
     const int64_t t0 = static_cast<int64_t>(tile) * kTile;
     for (int i = threadIdx.x; i < kTileWords * p.ncols; i += blockDim.x) bits[i] = 0u;
     load_tile_ids<KMAX>(p, t0, ids);
@@ -316,38 +295,30 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
     uint32_t* g_bits = p.tile_bits + static_cast<int64_t>(tile) * kTileWords * p.ncols;
     int* g_wpre = p.tile_wpre + static_cast<int64_t>(tile) * kTileWords * p.ncols;
     for (int i = threadIdx.x; i < kTileWords * p.ncols; i += blockDim.x) g_bits[i] = bits[i];
-
-    const bool publish = tile != p.suppress_tile;
-    unsigned long long* my_desc = p.desc + static_cast<int64_t>(tile) * p.ncols;
-    // aggregates first (all columns), so successors never wait on our look-back
+    // per column: word prefixes inside the tile, and the tile's count
     for (int col = threadIdx.x; col < p.ncols; col += blockDim.x) {
-      int n = 0;
-#pragma unroll
-      for (int j = 0; j < kTileWords; ++j) n += __popc(bits[j * p.ncols + col]);
-      if (publish) st_desc(&my_desc[col], pack_desc(p.epoch, tile == 0 ? kDescInclusive : kDescAggregate, n));
-    }
-    for (int col = threadIdx.x; col < p.ncols; col += blockDim.x) {
-      int run = tile > 0 ? lookback(p, tile, col, &timed_out) : 0;
-      s_run[col] = run;
       int n = 0;
 #pragma unroll
       for (int j = 0; j < kTileWords; ++j) {
-        g_wpre[j * p.ncols + col] = run + n;
+        g_wpre[j * p.ncols + col] = n;
         n += __popc(bits[j * p.ncols + col]);
       }
-      if (publish && tile > 0) st_desc(&my_desc[col], pack_desc(p.epoch, kDescInclusive, run + n));
-      if (tile == p.num_tiles - 1) p.totals[col] = run + n;
+      p.agg[static_cast<int64_t>(col) * p.num_tiles + tile] = n;
     }
     __syncthreads();  // before the next tile reuses shared memory (and for phase 2)
   }
-  if (timed_out) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
-  if (PROF && threadIdx.x == 0) t_phase1 = prof_now();
 
-  if (!grid_sync(p)) {
+  if (!grid_sync(p, 1)) {
     if (threadIdx.x == 0) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
     return;
   }
-  if (PROF && threadIdx.x == 0) t_barrier = prof_now();
+  if (PROF && threadIdx.x == 0) t_bar1 = prof_now();
+  column_scans(p);
+  if (!grid_sync(p, 2)) {
+    if (threadIdx.x == 0) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
+    return;
+  }
+  if (PROF && threadIdx.x == 0) t_bar2 = prof_now();
 
   // ---------------- phase 2: every plan array, all CTAs ----------------
   int* exp_off = s_run + p.ncols;               // [E+1]
@@ -355,7 +326,15 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   int* recv_off = pad_off + (p.E + 1);          // [P+1]
   int* s_slot = recv_off + (p.P + 1);           // [kTile * K] own tile's slots
   __shared__ int s_sizes[3];
-  if (threadIdx.x < 32) offsets_warp_scan(p, exp_off, pad_off, recv_off, s_sizes);
+  const bool own_tile = gridDim.x >= static_cast<unsigned>(p.num_tiles);
+  const bool has_tile = own_tile && blockIdx.x < static_cast<unsigned>(p.num_tiles);
+  if (threadIdx.x < 32) {
+    offsets_warp_scan(p, exp_off, pad_off, recv_off, s_sizes);
+  } else if (has_tile) {
+    // the own tile's exclusive prefix per column
+    for (int col = threadIdx.x - 32; col < p.ncols; col += blockDim.x - 32)
+      s_run[col] = __ldcg(&p.tile_pre[static_cast<int64_t>(col) * p.num_tiles + blockIdx.x]);
+  }
   __syncthreads();
   const int n_recv = s_sizes[kSizeRecv];
   const int n_exp = s_sizes[kSizeExp];
@@ -380,8 +359,6 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
   // need no global loads.  CTAs without a tile take the small passes.  (The
   // tile's [T,P] rows from shared memory too measured slower: the rows are
   // better spread over all CTAs.)
-  const bool own_tile = gridDim.x >= static_cast<unsigned>(p.num_tiles);
-  const bool has_tile = own_tile && blockIdx.x < static_cast<unsigned>(p.num_tiles);
   const int64_t extra = own_tile ? static_cast<int64_t>(gridDim.x - p.num_tiles) * blockDim.x : 0;
   // thread range of the small passes (negative: this thread takes none)
   const int64_t stid = extra > 0 ? gtid - static_cast<int64_t>(p.num_tiles) * blockDim.x : gtid;
@@ -429,7 +406,8 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
         pre[k] = 0;
         bw[k] = 0u;
         if (e[k] >= 0) {
-          pre[k] = __ldcg(&p.tile_wpre[word + e[k]]);
+          pre[k] = __ldcg(&p.tile_pre[static_cast<int64_t>(p.P + e[k]) * p.num_tiles + t]) +
+                   __ldcg(&p.tile_wpre[word + e[k]]);
           bw[k] = __ldcg(&p.tile_bits[word + e[k]]);
         }
       }
@@ -472,7 +450,8 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
         const int l0 = static_cast<int>(wq & (sub - 1)) * per;
         const int64_t at = tw * p.ncols + d;
         const uint32_t word = __ldcg(&p.tile_bits[at]);
-        int pos = __ldcg(&p.tile_wpre[at]) + __popc(word & lanes_below(l0));
+        int pos = __ldcg(&p.tile_pre[static_cast<int64_t>(d) * p.num_tiles + (tw / kTileWords)]) +
+                  __ldcg(&p.tile_wpre[at]) + __popc(word & lanes_below(l0));
         const int64_t g0 = tw * 32 + l0;
         const int n_tok = static_cast<int>(min64(per, p.T - g0));
         int t_local = static_cast<int>(static_cast<uint32_t>(g0) % static_cast<uint32_t>(p.S));
@@ -532,7 +511,7 @@ __global__ void __launch_bounds__(kTile) ep_plan_kernel(PlanDev p) {
     p.pad_rows[i] = row;
     p.exp_src[row] = -1;
   }
-  if (PROF) prof_cta_end(p, kProfPlan, t_start, t_scan, t_phase1, t_barrier, scanned, 0);
+  if (PROF) prof_cta_end(p, kProfPlan, t_start, t_scan, t_bar1, t_bar2, scanned, 0);
 }
 
 }  // namespace
@@ -566,7 +545,7 @@ int plan_grid(const PlanDev& p, int sm_budget) {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_plan_kernel<PROF, KMAX>, kTile, smem) != cudaSuccess ||
         per_sm < 1)
       return 0;
-    cached_per_sm = per_sm > 2 ? 2 : per_sm;
+    cached_per_sm = per_sm > kPlanThreadsPerSm / kTile ? kPlanThreadsPerSm / kTile : per_sm;
     cached_smem = smem;
   }
   const int sms = sm_budget > 0 && sm_budget < num_sms() ? sm_budget : num_sms();

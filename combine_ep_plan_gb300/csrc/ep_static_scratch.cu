@@ -1,7 +1,7 @@
 // ep_static_scratch.cu — ep_plan_static_scratch: the routing plan for callers
 // that cannot allocate device memory.
 //
-// ep_plan keeps its plan arrays and its scratch (look-back descriptors, tile
+// ep_plan keeps its plan arrays and its scratch (per-tile counts and prefixes, tile
 // ticket, done counter, status word, column totals) in one allocation that it
 // makes per handle.  Some callers cannot allocate at that point: a serving
 // runtime that reserved all device memory for its own arena at start-up, or a
@@ -75,15 +75,16 @@ extern "C" ep_status_t ep_plan_static_scratch(const int64_t* topk_idx, int64_t S
       !aligned4(out->slot) || !aligned4(out->exp_src) || !aligned4(out->pad_rows) || !aligned4(out->info))
     return EP_ERR_INVALID;
 
-  // Scratch layout: control words, look-back descriptors, tile bit matrices
+  // Scratch layout: control words, per-tile counts and prefixes, tile bit matrices
   // and word prefixes, sizes, column totals, padding offsets.
   const int ncols = P + E;
   const int num_tiles = static_cast<int>((T + ep::kTile - 1) / ep::kTile);
   const size_t tile_words = static_cast<size_t>(num_tiles) * ep::kTileWords * ncols;
   const size_t o_ctr = 0;
-  const size_t o_desc = round256(o_ctr + sizeof(unsigned) * ep::kCtrWords);
-  const size_t cleared = o_desc + sizeof(unsigned long long) * static_cast<size_t>(num_tiles) * ncols;
-  const size_t o_bits = round256(cleared);
+  const size_t cleared = sizeof(unsigned) * ep::kCtrWords;
+  const size_t o_agg = round256(cleared);
+  const size_t o_tpre = round256(o_agg + sizeof(int) * static_cast<size_t>(num_tiles) * ncols);
+  const size_t o_bits = round256(o_tpre + sizeof(int) * static_cast<size_t>(num_tiles) * ncols);
   const size_t o_wpre = round256(o_bits + sizeof(uint32_t) * tile_words);
   const size_t o_sizes = round256(o_wpre + sizeof(int) * tile_words);
   const size_t o_totals = round256(o_sizes + sizeof(int) * ep::kSizeWords);
@@ -97,8 +98,7 @@ extern "C" ep_status_t ep_plan_static_scratch(const int64_t* topk_idx, int64_t S
   char* base = static_cast<char*>(base_v);
 
   // Every call shares the scratch and finds the last call's contents in it:
-  // clear the control words and the look-back descriptors (the plan runs with
-  // epoch 1, which cleared descriptors never carry); the rest is overwritten.
+  // clear the control words; the rest is written before it is read.
   e = cudaMemsetAsync(base, 0, cleared, stream);
   if (e != cudaSuccess) return to_status(e);
 
@@ -116,8 +116,8 @@ extern "C" ep_status_t ep_plan_static_scratch(const int64_t* topk_idx, int64_t S
   p.ncols = ncols;
   p.topk_idx = topk_idx;
   p.ctr = reinterpret_cast<unsigned*>(base + o_ctr);
-  p.epoch = 1u;
-  p.desc = reinterpret_cast<unsigned long long*>(base + o_desc);
+  p.agg = reinterpret_cast<int*>(base + o_agg);
+  p.tile_pre = reinterpret_cast<int*>(base + o_tpre);
   p.tile_bits = reinterpret_cast<uint32_t*>(base + o_bits);
   p.tile_wpre = reinterpret_cast<int*>(base + o_wpre);
   p.sizes = reinterpret_cast<int*>(base + o_sizes);

@@ -329,7 +329,7 @@ ep_status_t ep_handle_destroy(ep_handle_t handle, ep_stream_t stream);
  * latency-critical loop where an allocation may block on the device or fail
  * under fragmentation.  It computes exactly what ep_plan computes, with the
  * same kernels, but writes every plan array into buffers the caller owns
- * (ep_plan_buffers_t) and keeps its scratch (look-back descriptors, counters,
+ * (ep_plan_buffers_t) and keeps its scratch (per-tile counts and prefixes, counters,
  * column totals) in one fixed array in the library's device memory,
  * EP_STATIC_SCRATCH_BYTES large, which every GPU that loads the library holds
  * until the process exits.  It calls no cudaMalloc, cudaFree or other
@@ -343,8 +343,8 @@ ep_status_t ep_handle_destroy(ep_handle_t handle, ep_stream_t stream);
  *   call's contents; each call clears what it needs.  Calls whose work
  *   overlaps on the GPU (other streams, other threads) race on the scratch:
  *   order them.
- * - Scratch need: about 0.28*T*(P+E) + 4*(P+2E) + 2 KB bytes (look-back
- *   descriptors, tile bit matrices and their word prefixes); a plan that
+ * - Scratch need: about 0.28*T*(P+E) + 4*(P+2E) + 2 KB bytes (per-tile
+ *   counts and prefixes, tile bit matrices and their word prefixes); a plan that
  *   would need more than EP_STATIC_SCRATCH_BYTES returns EP_ERR_CAPACITY
  *   before anything is enqueued (16384 tokens with P+E = 384 need about
  *   1.8 MB; 65536 tokens fit with P+E up to about 220).
@@ -428,7 +428,7 @@ ep_status_t ep_set_num_sms(ep_handle_t handle, int num_sms);
  * num_recv_host (may be NULL) receive N_exp and N_recv of a dispatch (0 for a
  * combine); asking for them makes a deferred dispatch wait on the host for
  * the plan.  Returns the status the device recorded up to the plan (an
- * invalid expert id, a look-back timeout) when the counts were read, else
+ * invalid expert id, a grid-barrier timeout) when the counts were read, else
  * EP_OK; later device errors (a capacity overflow in the scatter) are
  * returned by the next ep_sync_status.  Every pending object must be waited
  * on exactly once, before its handle is destroyed, and the buffers it uses
@@ -479,14 +479,14 @@ ep_status_t ep_profile_end(ep_handle_t handle, int64_t *records_written_host,
                            int64_t *records_dropped_host);
 
 /*
- * ep_debug_set_lookback — test hook for the bounded wait of the plan's
- * single-pass scan.  poll_limit > 0 sets how many times a tile polls a
- * predecessor's descriptor before it gives up and records EP_ERR_TIMEOUT
- * (0 restores the default); suppress_tile >= 0 makes that tile never publish
- * its descriptors, so that its successor's wait runs out (-1 disables).
+ * ep_debug_set_plan_wait — test hook for the bounded waits of the plan's two
+ * grid barriers.  poll_limit > 0 sets how many times a CTA polls the
+ * barrier before it gives up and records EP_ERR_TIMEOUT (0 restores the
+ * default); suppress_tile >= 0 makes the CTA of that tile return before the
+ * first barrier, so that the others' wait runs out (-1 disables).
  * Process-wide; affects plans enqueued afterwards.
  */
-void ep_debug_set_lookback(int64_t poll_limit, int suppress_tile);
+void ep_debug_set_plan_wait(int64_t poll_limit, int suppress_tile);
 
 #ifdef __cplusplus
 }

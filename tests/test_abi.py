@@ -43,7 +43,7 @@ def test_header_declares_the_boundary():
 def test_every_declared_symbol_is_exported(lib):
     missing = [n for n in declared_functions() if not hasattr(lib, n)]
     assert not missing, missing
-    assert lib.ep_abi_version() == 3
+    assert lib.ep_abi_version() == 4
 
 
 def test_status_strings(lib):

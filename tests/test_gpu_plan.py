@@ -130,21 +130,26 @@ def test_device_reports_invalid_routing(mutate):
     assert h.sync_status() == ep.EP_OK  # cleared
 
 
-def test_lookback_timeout_is_reported_and_recoverable():
-    """A tile that never publishes makes its successor's bounded wait run out:
-    the plan reports EP_ERR_TIMEOUT and the next plan succeeds."""
+def test_barrier_timeout_is_reported_and_recoverable():
+    """A tile whose CTA never arrives at the first grid barrier makes the
+    others' bounded wait run out: the plan reports EP_ERR_TIMEOUT and the
+    next plan succeeds."""
     w = WORKLOADS["bf16"].scaled(S=200)  # 1600 tokens -> 7 tiles
     idx, _ = draw_topk(w)
     t = torch.from_numpy(idx).cuda()
     try:
-        ep.set_lookback_debug(poll_limit=2000, suppress_tile=2)
+        ep.set_plan_wait_debug(poll_limit=2000, suppress_tile=2)
         h = ep.plan(t, w.P, w.E, w.A)
         assert h.sync_status() == ep.EP_ERR_TIMEOUT
     finally:
-        ep.set_lookback_debug(0, -1)
+        ep.set_plan_wait_debug(0, -1)
     h2 = ep.plan(t, w.P, w.E, w.A)
     assert h2.sync_status() == ep.EP_OK
     assert_plan_equal(gpu_plan_arrays(h2), oracle.plan(idx, w.S, w.P, w.E, w.A))
+    # the handle that timed out recovers too
+    h.replan(t)
+    assert h.sync_status() == ep.EP_OK
+    assert_plan_equal(gpu_plan_arrays(h), oracle.plan(idx, w.S, w.P, w.E, w.A))
 
 
 def test_worst_expanded_rows_bounds_exact_size():
