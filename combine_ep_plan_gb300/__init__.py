@@ -613,8 +613,8 @@ def summarize_profile(records) -> list:
     in launch order: kernel, CTAs, units, payload bytes, span from the first
     CTA start to the last CTA end (ns), median and max CTA duration (ns),
     payload GB/s over the span, and for the plan the median stage offsets
-    from the launch's first start, in ns: route scan and end of phase 1 over
-    the CTAs that scanned a tile, grid barrier passed over all CTAs."""
+    from the launch's first start, in ns: route scan over the CTAs that
+    scanned a tile, each grid barrier passed over all CTAs."""
     import numpy as np
     r = np.asarray(records.cpu() if isinstance(records, torch.Tensor) else records).astype(np.uint64)
     if r.size == 0:
@@ -634,12 +634,12 @@ def summarize_profile(records) -> list:
                "cta_ns_median": float(np.median(t1 - t0)), "cta_ns_max": int((t1 - t0).max()),
                "gbs": nbytes / span if span > 0 else 0.0}
         if k == 1:
-            # route scan and end of phase 1 over the CTAs that scanned a tile
-            # (the others have no scan mark); the barrier over all CTAs
+            # route scan over the CTAs that scanned a tile (the others have
+            # no scan mark); the two grid barriers over all CTAs
             base = t0.min()
             tiles = r[m, 2] > 0
-            for name, col, sel in (("scan_ns", 2, tiles), ("phase1_ns", 3, tiles),
-                                   ("barrier_ns", 4, np.ones_like(tiles))):
+            for name, col, sel in (("scan_ns", 2, tiles), ("barrier1_ns", 3, np.ones_like(tiles)),
+                                   ("barrier2_ns", 4, np.ones_like(tiles))):
                 v = r[m, col].astype(np.int64)[sel]
                 v = v[v > 0]
                 row[name] = float(np.median(v - base)) if len(v) else 0.0

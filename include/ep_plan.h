@@ -466,7 +466,8 @@ ep_status_t ep_pending_wait(ep_pending_t pending, int64_t *num_expanded_host,
  *       pre-quantised FP8, 5 combine, 6 dispatch backward
  *   [1] start, [5] end: device global timer, ns
  *   [2] [3] [4] stage marks (plan: route scan of the CTA's last tile done,
- *       phase 1 done, grid barrier passed; 0 for the other kernels)
+ *       first grid barrier passed, second grid barrier passed; 0 for the
+ *       other kernels)
  *   [6] work units: plan, tokens scanned; others, (row, column chunk) items
  *   [7] payload bytes read and written by the CTA (hidden rows, codes, scales,
  *       bias; 0 for the plan)

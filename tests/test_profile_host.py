@@ -24,9 +24,9 @@ def test_summary_groups_by_launch_in_order():
     assert plan["ctas"] == 3 and plan["units"] == 356 and plan["bytes"] == 0
     assert plan["span_ns"] == 4000 - 1000
     # stage marks: medians of the non-zero marks, from the launch's first start
-    assert plan["scan_ns"] == np.median([500, 600])
-    assert plan["phase1_ns"] == np.median([1000, 1100])  # CTAs with a tile only
-    assert plan["barrier_ns"] == np.median([1600, 1600, 1610])
+    assert plan["scan_ns"] == np.median([500, 600])  # CTAs with a tile only
+    assert plan["barrier1_ns"] == np.median([1000, 1100, 30])
+    assert plan["barrier2_ns"] == np.median([1600, 1600, 1610])
     assert disp["ctas"] == 2 and disp["units"] == 14 and disp["bytes"] == 16000
     assert disp["span_ns"] == 2000 and disp["gbs"] == 8.0
     assert disp["cta_ns_median"] == np.median([1000, 1900]) and disp["cta_ns_max"] == 1900
