@@ -235,11 +235,12 @@ class EPHandle:
         _check(_lib().ep_profile_begin(self.ptr, self._prof.data_ptr(), capacity), "ep_profile_begin")
 
     def profile_end(self, stream: Optional[torch.cuda.Stream] = None):
-        """Stop recording; synchronise `stream` and return (records [n, 8]
+        """Stop recording; synchronise the device (the launches may have run
+        on the handle's communication stream) and return (records [n, 8]
         int64 on the host, dropped count)."""
         n, dropped = ctypes.c_int64(), ctypes.c_int64()
         _check(_lib().ep_profile_end(self.ptr, ctypes.byref(n), ctypes.byref(dropped)), "ep_profile_end")
-        (stream or torch.cuda.current_stream()).synchronize()
+        torch.cuda.synchronize(self.device)
         rec = self._prof[: n.value].cpu()
         self._prof = None
         return rec, dropped.value
