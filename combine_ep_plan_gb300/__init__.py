@@ -513,7 +513,7 @@ class Pending:
     def wait(self, counts: bool = True):
         """dispatch: (recv_x, recv_scales|None, N_exp, N_recv); combine: out.
         counts=False skips the count readback (no host wait; N_exp and N_recv
-        are then returned as 0 unless the issue already read them)."""
+        are then returned as 0)."""
         if not self._ptr:
             raise RuntimeError("pending call already waited on")
         ne, nr = ctypes.c_int64(), ctypes.c_int64()

@@ -302,3 +302,53 @@ def test_profile_drops_what_does_not_fit():
     cta = (rec.numpy().astype(np.uint64)[:, 0] & np.uint64(0xFFFFFFFF)).astype(np.int64)
     assert np.array_equal(cta, np.arange(8))
     h.check()
+
+
+def test_profile_records_of_async_calls():
+    """Launches issued on the communication stream write their records too."""
+    w = CASES[1]
+    idx, wts, x = _inputs(w)
+    pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
+    idx_t = torch.from_numpy(idx).cuda()
+    h = ep.plan(idx_t, w.P, w.E, w.A)
+    h.profile_begin(1 << 16)
+    recv, _, n_exp, _ = ep.dispatch_async(h, bits_to_bf16_tensor(x).cuda(), topk_idx=idx_t).wait()
+    out = ep.combine_async(h, recv, torch.from_numpy(wts).cuda()).wait()
+    rec, dropped = h.profile_end()
+    assert dropped == 0
+    kinds = [r["kernel"] for r in ep.summarize_profile(rec)]
+    assert kinds == ["plan", "dispatch_bf16", "combine"]
+    assert np.array_equal(u16(recv)[:n_exp], oracle.dispatch_bf16(x, pl))
+    assert np.array_equal(u16(out), oracle.combine(oracle.dispatch_bf16(x, pl), pl, wts))
+    h.check()
+
+
+@pytest.mark.parametrize("defer", [False, True])
+def test_combine_async_matches_sync(defer):
+    w = CASES[2]
+    idx, wts, x = _inputs(w)
+    pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
+    h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
+    y = bits_to_bf16_tensor(draw_y(pl.num_expanded, w.H, 12)).cuda()
+    wts_t = torch.from_numpy(wts).cuda()
+    ref = u16(ep.combine(h, y, wts_t))
+    got = u16(ep.combine_async(h, y, wts_t, defer_epilogue=defer).wait())
+    assert np.array_equal(got, ref)
+    assert np.array_equal(got, oracle.combine(u16(y), pl, wts))
+
+
+def test_wait_without_counts():
+    """A dispatch waited on without counts joins the stream only (the counts
+    come back as 0); the rows are there either way."""
+    w = CASES[1]
+    idx, _, x = _inputs(w)
+    pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
+    h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
+    x_t = bits_to_bf16_tensor(x).cuda()
+    recv, _, n_exp, n_recv = ep.dispatch_async(h, x_t, defer_epilogue=True).wait(counts=False)
+    assert (n_exp, n_recv) == (0, 0)
+    assert np.array_equal(u16(recv)[:pl.num_expanded], oracle.dispatch_bf16(x, pl))
+    recv, _, n_exp, n_recv = ep.dispatch_async(h, x_t, defer_epilogue=False).wait(counts=False)
+    assert (n_exp, n_recv) == (0, 0)
+    assert np.array_equal(u16(recv)[:pl.num_expanded], oracle.dispatch_bf16(x, pl))
+    h.check()
