@@ -46,6 +46,23 @@ __device__ __forceinline__ int64_t scale_at(const DispatchDev& a, int64_t r, int
 // kernel, plus a per-CTA record (items, payload bytes, start and end).
 template <int ROW_DIV, bool WITH_SCALES, bool PROF>
 __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
+  // Before anything else, even before the wait for the previous kernel: one
+  // bulk L2 prefetch of the warp's first source chunk (token items only; x
+  // is an input, never written by the plan), so that the row is on its way
+  // while the plan outputs are read.  Measured 2.8 us faster per bf16 step.
+  {
+    const int64_t hv = a.H / ROW_DIV;
+    constexpr int kChunk = 32 * kUnroll;
+    const int64_t chunks = (hv + kChunk - 1) / kChunk;
+    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    if ((threadIdx.x & 31) == 0 && w < a.T * chunks) {
+      const int64_t ri = w / chunks;
+      const int64_t v0 = (w - ri * chunks) * kChunk;
+      const unsigned n = static_cast<unsigned>((hv - v0 < kChunk ? hv - v0 : kChunk) * 16);
+      const uint4* src = static_cast<const uint4*>(a.x) + ri * hv + v0;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(n) : "memory");
+    }
+  }
   pdl_wait();
   unsigned long long t0 = 0, units = 0, bytes = 0;
   if (PROF && threadIdx.x == 0) t0 = prof_now();
