@@ -226,7 +226,8 @@ ep_status_t enqueue_plan(ep_handle_s* h, const int64_t* topk_idx, cudaStream_t s
   Launch L(h);
   L.target(h->dev);
   const cudaError_t e = ep::launch_plan(h->dev, stream, L.cfg);
-  if (e == cudaSuccess) h->bar_count += 2u * static_cast<unsigned>(L.ctas);  // two barriers
+  // two barriers, each one arrival per CTA (a one-CTA plan uses neither)
+  if (e == cudaSuccess && L.ctas > 1) h->bar_count += 2u * static_cast<unsigned>(L.ctas);
   return cuda_status(finish_launch(h, L, e));
 }
 

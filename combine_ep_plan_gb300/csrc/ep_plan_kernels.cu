@@ -102,6 +102,10 @@ __device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids
 // the one reduction, seen by each poller one load later.
 __device__ bool grid_sync(const PlanDev& p, unsigned round) {
   __shared__ int s_ok;
+  if (gridDim.x == 1) {  // a one-CTA plan: the CTA barrier orders everything
+    __syncthreads();
+    return true;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
     unsigned* count = p.ctr + kCtrBarCount;
@@ -550,6 +554,7 @@ int plan_grid(const PlanDev& p, int sm_budget) {
   }
   const int sms = sm_budget > 0 && sm_budget < num_sms() ? sm_budget : num_sms();
   const int64_t cap = static_cast<int64_t>(cached_per_sm) * sms;
+  if (p.num_tiles == 1) return 1;  // one tile: one CTA, no grid barrier, no cooperative launch
   const int64_t work = p.T * (p.K + p.P) + static_cast<int64_t>(p.P) * p.P * p.C + static_cast<int64_t>(p.P) * p.E;
   int64_t grid = (work + EP_PLAN_WORK_PER_CTA - 1) / EP_PLAN_WORK_PER_CTA;
   if (grid < p.num_tiles) grid = p.num_tiles;
@@ -567,6 +572,11 @@ cudaError_t launch_plan_t(const PlanDev& p, cudaStream_t stream, const LaunchCfg
   }
   const int grid = plan_grid<PROF, KMAX>(p, cfg.sm_budget);
   if (grid < 1) return cudaErrorInvalidConfiguration;
+  if (grid == 1) {
+    if (cfg.ctas) *cfg.ctas = 1;
+    ep_plan_kernel<PROF, KMAX><<<1, kTile, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
   PlanDev arg = p;
   void* args[] = {&arg};
   if (cfg.ctas) *cfg.ctas = grid;
