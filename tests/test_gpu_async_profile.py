@@ -352,3 +352,23 @@ def test_wait_without_counts():
     assert (n_exp, n_recv) == (0, 0)
     assert np.array_equal(u16(recv)[:pl.num_expanded], oracle.dispatch_bf16(x, pl))
     h.check()
+
+
+def test_one_tile_plan_profile_and_replan():
+    """A plan of one tile runs as one CTA without grid barriers; its record,
+    and plans before and after it on the same handle, stay right."""
+    w = WORKLOADS["tiny"]  # 256 tokens: one tile
+    idx, _, _ = _inputs(w)
+    idx2, _, _ = _inputs(w, seed=5)
+    t, t2 = torch.from_numpy(idx).cuda(), torch.from_numpy(idx2).cuda()
+    h = ep.plan(t, w.P, w.E, w.A)
+    h.profile_begin(64)
+    h.replan(t2)
+    rec, dropped = h.profile_end()
+    s = ep.summarize_profile(rec)
+    assert dropped == 0 and len(s) == 1 and s[0]["kernel"] == "plan"
+    assert s[0]["ctas"] == 1 and s[0]["units"] == w.T
+    assert_plan_equal(gpu_plan_arrays(h), oracle.plan(idx2, w.S, w.P, w.E, w.A))
+    h.replan(t)
+    assert_plan_equal(gpu_plan_arrays(h), oracle.plan(idx, w.S, w.P, w.E, w.A))
+    h.check()
