@@ -204,9 +204,11 @@ class EPHandle:
         view = _ArrayView(p.value, list(shape)[: nd.value], _TYPESTR[dtype])
         return torch.as_tensor(view, device=f"cuda:{self.device}")
 
-    def sizes(self, stream: Optional[torch.cuda.Stream] = None) -> Tuple[int, int]:
-        """(N_exp, N_recv); synchronises the stream on first call."""
-        if self._sizes is None:
+    def sizes(self, stream: Optional[torch.cuda.Stream] = None, refresh: bool = False) -> Tuple[int, int]:
+        """(N_exp, N_recv); synchronises the stream on the first call after a
+        plan made through this object.  refresh=True reads them again (after
+        plans this object did not see, such as replays of a captured graph)."""
+        if self._sizes is None or refresh:
             ne, nr = ctypes.c_int64(), ctypes.c_int64()
             _check(_lib().ep_plan_sizes(self.ptr, _stream_ptr(stream), ctypes.byref(ne), ctypes.byref(nr)),
                    "ep_plan_sizes")

@@ -48,7 +48,6 @@ struct ep_handle_s {
   size_t zero_bytes = 0;
   int64_t cap_recv = 0, cap_exp = 0, cap_pad = 0;
   int device = 0;
-  unsigned bar_count = 0;  // grid-barrier arrivals of this handle's plans so far
   // SM budget of the dispatch, combine and backward launches (0 = all)
   int sm_budget = 0;
   // asynchronous calls: communication stream, pinned count slots in use,
@@ -222,12 +221,9 @@ ep_status_t enqueue_plan(ep_handle_s* h, const int64_t* topk_idx, cudaStream_t s
   h->dev.topk_idx = topk_idx;
   h->dev.poll_limit = g_poll_limit;
   h->dev.suppress_tile = g_suppress_tile;
-  h->dev.bar_base = h->bar_count;
   Launch L(h);
   L.target(h->dev);
   const cudaError_t e = ep::launch_plan(h->dev, stream, L.cfg);
-  // two barriers, each one arrival per CTA (a one-CTA plan uses neither)
-  if (e == cudaSuccess && L.ctas > 1) h->bar_count += 2u * static_cast<unsigned>(L.ctas);
   return cuda_status(finish_launch(h, L, e));
 }
 
@@ -242,11 +238,10 @@ ep_status_t read_status_word(ep_handle_s* h, cudaStream_t stream, bool clear, in
     if (e != cudaSuccess) return cuda_status(e);
   }
   if (clear && st) {
-    // after a timed-out wait the barrier count may be short: reset it too
+    // after a timed-out wait the barrier counts may be off: reset them too
     const unsigned zeros[ep::kCtrWords] = {};
     if (st & ep::kStTimeout) {
       e = cudaMemcpy(h->dev.ctr, zeros, sizeof zeros, cudaMemcpyHostToDevice);
-      h->bar_count = 0;
     } else {
       e = cudaMemcpy(h->dev.ctr + ep::kCtrStatus, zeros, sizeof(unsigned), cudaMemcpyHostToDevice);
     }

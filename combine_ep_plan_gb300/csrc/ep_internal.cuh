@@ -21,12 +21,14 @@ constexpr unsigned kStCapacity = 4u;    // an output row at or beyond capacity
 constexpr unsigned kStTimeout = 8u;     // a bounded grid-barrier wait gave up
 
 // Control words (zeroed when a handle is created), each in its own 128-byte
-// line.  The grid barriers' arrival count is never reset: a plan's barrier
-// r (1 or 2) waits for it to reach bar_base + r * its grid size, bar_base
-// being the arrivals of the handle's earlier plans (kept on the host).
-constexpr int kCtrBarCount = 0;   // grid barrier: CTAs arrived, all plans
-constexpr int kCtrStatus = 32;    // device status word
-constexpr int kCtrWords = 64;
+// line.  A plan's grid barrier r (1 or 2) waits for the arrival count to
+// reach r times its grid size; each CTA then departs, and the last to
+// depart sets both counts back to zero, so every launch (and every replay
+// of a captured launch) starts from zero.
+constexpr int kCtrBarCount = 0;    // grid barriers: CTAs arrived
+constexpr int kCtrBarDepart = 32;  // CTAs past the last barrier
+constexpr int kCtrStatus = 64;     // device status word
+constexpr int kCtrWords = 96;
 
 // Size slots.
 constexpr int kSizeRecv = 0;  // N_recv
@@ -185,8 +187,6 @@ struct PlanDev {
   int* exp_src;        // [T*K + E*(A-1)]
   int* pad_rows;       // [E*(A-1)]
   unsigned char* in_rank;  // [T,P]
-  // arrivals at the grid barriers before this plan (see kCtrBarCount)
-  unsigned bar_base;
   // bounded wait of the grid barriers, and a test hook (a tile whose CTA
   // returns before the first barrier)
   long long poll_limit;

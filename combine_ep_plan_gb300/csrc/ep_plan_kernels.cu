@@ -97,9 +97,9 @@ __device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids
 
 // Bounded grid-wide barrier for a cooperative launch.  Each CTA adds one
 // arrival (a release reduction: nothing to wait for) and polls the count
-// until it reaches this barrier's target, the arrivals of the handle's
-// earlier plans plus `round` times the grid: the release of the last CTA is
-// the one reduction, seen by each poller one load later.
+// until it reaches `round` times the grid: the release of the last CTA is
+// the one reduction, seen by each poller one load later.  grid_depart
+// resets the count once every CTA is past the last barrier.
 __device__ bool grid_sync(const PlanDev& p, unsigned round) {
   __shared__ int s_ok;
   if (gridDim.x == 1) {  // a one-CTA plan: the CTA barrier orders everything
@@ -109,7 +109,7 @@ __device__ bool grid_sync(const PlanDev& p, unsigned round) {
   __syncthreads();
   if (threadIdx.x == 0) {
     unsigned* count = p.ctr + kCtrBarCount;
-    const unsigned target = p.bar_base + round * gridDim.x;
+    const unsigned target = round * gridDim.x;
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
     int ok = 1;
     long long polls = 0;
@@ -126,6 +126,17 @@ __device__ bool grid_sync(const PlanDev& p, unsigned round) {
   }
   __syncthreads();
   return s_ok != 0;
+}
+
+// After the last barrier: the last CTA to depart zeroes both counts (no CTA
+// still polls then), so the next launch of the plan starts from zero.
+__device__ void grid_depart(const PlanDev& p) {
+  if (gridDim.x == 1 || threadIdx.x != 0) return;
+  unsigned* depart = p.ctr + kCtrBarDepart;
+  if (atomicAdd(depart, 1u) == gridDim.x - 1) {
+    p.ctr[kCtrBarCount] = 0u;
+    *depart = 0u;
+  }
 }
 
 // Column scans, one warp per column: the tiles' counts in order, 32 at a
@@ -323,6 +334,7 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
     return;
   }
   if (PROF && threadIdx.x == 0) t_bar2 = prof_now();
+  grid_depart(p);
 
   // ---------------- phase 2: every plan array, all CTAs ----------------
   int* exp_off = s_run + p.ncols;               // [E+1]

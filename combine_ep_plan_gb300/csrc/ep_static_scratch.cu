@@ -136,7 +136,6 @@ extern "C" ep_status_t ep_plan_static_scratch(const int64_t* topk_idx, int64_t S
   p.exp_src = out->exp_src;
   p.pad_rows = out->pad_rows;
   p.in_rank = out->is_token_in_rank;
-  p.bar_base = 0;  // the control words were just cleared
   p.poll_limit = 1ll << 20;
   p.suppress_tile = -1;
 

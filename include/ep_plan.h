@@ -21,6 +21,12 @@
  *     returned by the next synchronising call (ep_plan_sizes, ep_sync_status).
  *   - A handle is not thread-safe; calls that use one handle on different
  *     streams must be ordered by the caller.
+ *   - ep_replan, ep_dispatch, ep_dispatch_cached, ep_dispatch_metadata,
+ *     ep_combine and the backward calls may be captured in a CUDA graph and
+ *     replayed (the plan's grid barriers reset their counts at the end of
+ *     every launch); the asynchronous calls and ep_plan_sizes may not.
+ *     Profile records of captured launches land at the capture-time
+ *     positions on every replay.
  *
  * Sources are cited by page title and section:
  *   [DO] "Ascend DeepEP MoE Dispatch Optimization"
