@@ -21,14 +21,16 @@ constexpr unsigned kStCapacity = 4u;    // an output row at or beyond capacity
 constexpr unsigned kStTimeout = 8u;     // a bounded grid-barrier wait gave up
 
 // Control words (zeroed when a handle is created), each in its own 128-byte
-// line.  A plan's grid barrier r (1 or 2) waits for the arrival count to
-// reach r times its grid size; each CTA then departs, and the last to
-// depart sets both counts back to zero, so every launch (and every replay
-// of a captured launch) starts from zero.
-constexpr int kCtrBarCount = 0;    // grid barriers: CTAs arrived
-constexpr int kCtrBarDepart = 32;  // CTAs past the last barrier
-constexpr int kCtrStatus = 64;     // device status word
-constexpr int kCtrWords = 96;
+// line.  The grid barriers use one of two arrival counts, picked by the
+// parity of a generation word every CTA reads when the plan starts; after
+// the second barrier CTA 0 zeroes the other count and bumps the generation,
+// so each launch (and each replay of a captured launch) finds a zeroed count
+// and leaves one for the next.
+constexpr int kCtrBarCount = 0;   // grid barriers: CTAs arrived, generation 0, 2, ...
+constexpr int kCtrBarCount1 = 32; // ... generation 1, 3, ...
+constexpr int kCtrBarGen = 64;    // generation
+constexpr int kCtrStatus = 96;    // device status word
+constexpr int kCtrWords = 128;
 
 // Size slots.
 constexpr int kSizeRecv = 0;  // N_recv

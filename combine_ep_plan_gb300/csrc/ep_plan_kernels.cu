@@ -96,11 +96,11 @@ __device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids
 }
 
 // Bounded grid-wide barrier for a cooperative launch.  Each CTA adds one
-// arrival (a release reduction: nothing to wait for) and polls the count
-// until it reaches `round` times the grid: the release of the last CTA is
-// the one reduction, seen by each poller one load later.  grid_depart
-// resets the count once every CTA is past the last barrier.
-__device__ bool grid_sync(const PlanDev& p, unsigned round) {
+// arrival to this launch's count (a release reduction: nothing to wait for)
+// and polls it until it reaches `round` times the grid: the release of the
+// last CTA is the one reduction, seen by each poller one load later.
+// `count` is meaningful in thread 0 only.
+__device__ bool grid_sync(const PlanDev& p, unsigned* count, unsigned round) {
   __shared__ int s_ok;
   if (gridDim.x == 1) {  // a one-CTA plan: the CTA barrier orders everything
     __syncthreads();
@@ -108,7 +108,6 @@ __device__ bool grid_sync(const PlanDev& p, unsigned round) {
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    unsigned* count = p.ctr + kCtrBarCount;
     const unsigned target = round * gridDim.x;
     asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
     int ok = 1;
@@ -126,17 +125,6 @@ __device__ bool grid_sync(const PlanDev& p, unsigned round) {
   }
   __syncthreads();
   return s_ok != 0;
-}
-
-// After the last barrier: the last CTA to depart zeroes both counts (no CTA
-// still polls then), so the next launch of the plan starts from zero.
-__device__ void grid_depart(const PlanDev& p) {
-  if (gridDim.x == 1 || threadIdx.x != 0) return;
-  unsigned* depart = p.ctr + kCtrBarDepart;
-  if (atomicAdd(depart, 1u) == gridDim.x - 1) {
-    p.ctr[kCtrBarCount] = 0u;
-    *depart = 0u;
-  }
 }
 
 // Column scans, one warp per column: the tiles' counts in order, 32 at a
@@ -289,6 +277,9 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
   extern __shared__ __align__(16) uint32_t smem[];
   unsigned long long t_start = 0, t_scan = 0, t_bar1 = 0, t_bar2 = 0, scanned = 0;
   if (PROF && threadIdx.x == 0) t_start = prof_now();
+  // this launch's barrier count (thread 0; the read is first used at barrier 1)
+  const unsigned gen = threadIdx.x == 0 ? __ldcg(&p.ctr[kCtrBarGen]) : 0u;
+  unsigned* bar_count = p.ctr + ((gen & 1u) ? kCtrBarCount1 : kCtrBarCount);
 
   // ---------------- phase 1: tiles ----------------
   uint32_t* bits = smem;                                           // [kTileWords * ncols]
@@ -323,18 +314,22 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
     __syncthreads();  // before the next tile reuses shared memory (and for phase 2)
   }
 
-  if (!grid_sync(p, 1)) {
+  if (!grid_sync(p, bar_count, 1)) {
     if (threadIdx.x == 0) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
     return;
   }
   if (PROF && threadIdx.x == 0) t_bar1 = prof_now();
   column_scans(p);
-  if (!grid_sync(p, 2)) {
+  if (!grid_sync(p, bar_count, 2)) {
     if (threadIdx.x == 0) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
     return;
   }
   if (PROF && threadIdx.x == 0) t_bar2 = prof_now();
-  grid_depart(p);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && gridDim.x > 1) {
+    // nobody uses the other count in this launch: zero it for the next one
+    p.ctr[(gen & 1u) ? kCtrBarCount : kCtrBarCount1] = 0u;
+    p.ctr[kCtrBarGen] = gen + 1u;
+  }
 
   // ---------------- phase 2: every plan array, all CTAs ----------------
   int* exp_off = s_run + p.ncols;               // [E+1]

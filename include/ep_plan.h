@@ -23,8 +23,8 @@
  *     streams must be ordered by the caller.
  *   - ep_replan, ep_dispatch, ep_dispatch_cached, ep_dispatch_metadata,
  *     ep_combine and the backward calls may be captured in a CUDA graph and
- *     replayed (the plan's grid barriers reset their counts at the end of
- *     every launch); the asynchronous calls and ep_plan_sizes may not.
+ *     replayed (the plan's grid barriers leave a zeroed count for the next
+ *     launch); the asynchronous calls and ep_plan_sizes may not.
  *     Profile records of captured launches land at the capture-time
  *     positions on every replay.
  *
