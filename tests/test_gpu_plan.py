@@ -170,3 +170,27 @@ def test_new_handle_on_reused_pool_memory():
         h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
         assert_plan_equal(gpu_plan_arrays(h), oracle.plan(idx, w.S, w.P, w.E, w.A))
         h.destroy()
+
+
+def test_many_replans_with_changing_grids():
+    """Hundreds of plans on one handle, the grid changing between them (SM
+    budgets, profiling variants): every barrier must start from a zeroed
+    count; spot checks against the oracle."""
+    w = WORKLOADS["bf16"].scaled(S=300)  # 10 tiles
+    h = None
+    for i in range(240):
+        idx, _ = draw_topk(w, seed=1000 + (i % 7))
+        t = torch.from_numpy(idx).cuda()
+        if h is None:
+            h = ep.plan(t, w.P, w.E, w.A)
+        h.set_num_sms([0, 3, 17, 152][i % 4])
+        if i % 5 == 0:
+            h.profile_begin(4096)
+            h.replan(t)
+            h.profile_end()
+        else:
+            h.replan(t)
+        if i % 37 == 0 or i == 239:
+            assert h.sync_status() == ep.EP_OK
+            assert_plan_equal(gpu_plan_arrays(h), oracle.plan(idx, w.S, w.P, w.E, w.A))
+    assert h.sync_status() == ep.EP_OK
