@@ -162,8 +162,8 @@ def test_worst_expanded_rows_bounds_exact_size():
 
 def test_new_handle_on_reused_pool_memory():
     """A handle made right after another one was destroyed gets the same pool
-    memory back, stale look-back descriptors included: its plan must ignore
-    them."""
+    memory back, stale barrier counts and scratch included: its plans must
+    not depend on what that memory held."""
     w = WORKLOADS["bf16"].scaled(S=300)
     for seed in range(4):
         idx, _ = draw_topk(w, seed=100 + seed)

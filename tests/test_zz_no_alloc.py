@@ -100,7 +100,7 @@ def test_static_scratch_plan_matches_ep_plan_twice_in_a_row(lib, name):
 
 
 def test_static_scratch_rejects_plans_beyond_its_limit(lib):
-    # 2^20 tokens with P+E = 2048 would need 64 MB of look-back descriptors
+    # 2^20 tokens with P+E = 2048 would need over 500 MB of tile bit matrices and prefixes
     w = WORKLOADS["tiny"].scaled(P=64, E=1984, S=16384, K=2, A=1)
     st = PlanBuffers(**{f: 1 << 20 for f, _ in PlanBuffers._fields_})  # never dereferenced
     rc = lib.ep_plan_static_scratch(1 << 20, w.S, w.P, w.K, w.E, w.A, 0, ctypes.byref(st), None)
