@@ -19,8 +19,12 @@ from dataclasses import dataclass
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "ep_oracle.c")
-_LIB = os.path.join(_HERE, "libep_oracle.so")
+# EP_ORACLE_SOURCE: a modified copy of ep_oracle.c to build and load instead
+# (the planted-mistake test runs the pins against such copies); its library
+# is written next to it.
+_SRC = os.environ.get("EP_ORACLE_SOURCE") or os.path.join(_HERE, "ep_oracle.c")
+_LIB = (os.path.splitext(_SRC)[0] + ".so" if os.environ.get("EP_ORACLE_SOURCE")
+        else os.path.join(_HERE, "libep_oracle.so"))
 
 OK = 0
 ERR_INVALID = 1
@@ -35,11 +39,11 @@ class OracleError(RuntimeError):
 
 
 def build(force: bool = False) -> str:
-    """Compile ep_oracle.c into libep_oracle.so next to it (atomic rename)."""
+    """Compile the oracle source into its library next to it (atomic rename)."""
     if (not force and os.path.exists(_LIB)
             and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
         return _LIB
-    fd, tmp = tempfile.mkstemp(suffix=".so", dir=_HERE)
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(_LIB))
     os.close(fd)
     cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
            "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]

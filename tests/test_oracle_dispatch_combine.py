@@ -80,6 +80,28 @@ def test_fp8_dequant_error_bound():
     assert np.all(err <= bound)
 
 
+def test_fp8_dequant_expert_matches_library_casts():
+    """The dequantising identity expert, y = bf16_RNE(float(q) * scale of the
+    element's group), against torch's E4M3 decode and bf16 cast on the FP8
+    rows of a dispatch; it also stays within the E4M3 bound of the source
+    rows plus one bf16 rounding."""
+    w = CASES[2]
+    idx, wts, x, pl = _setup(w)
+    q, sc = oracle.dispatch_fp8(x, pl)
+    y = oracle.expert_dequant(q, sc)
+    G = w.H // 128
+    dec = torch.from_numpy(q).view(torch.float8_e4m3fn).float().numpy().reshape(-1, G, 128)
+    prod = (dec * sc[..., None]).astype(np.float32).reshape(-1, w.H)  # one fp32 product
+    assert np.array_equal(y, _f32_to_bf16_bits(prod))
+    real = pl.exp_src >= 0
+    yr = _bf16_to_f32(y[real]).reshape(-1, G, 128).astype(np.float64)
+    xr = _bf16_to_f32(x[pl.exp_src[real]]).reshape(-1, G, 128)
+    s = sc[real][..., None].astype(np.float64)
+    bound = (2.0 ** -4 * np.abs(xr) + 2.0 ** -10 * s) * (1 + 1e-6) + 2.0 ** -8 * np.abs(yr)
+    assert np.all(np.abs(yr - xr) <= bound)
+    assert not y[~real].any()
+
+
 def test_fp8_zero_group_special_case():
     w = WORKLOADS["tiny"].scaled(H=256)
     idx, wts, x, pl = _setup(w)
