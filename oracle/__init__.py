@@ -160,6 +160,16 @@ def validate(topk_idx: np.ndarray, S: int, P: int, E: int, A: int, C: int = 0) -
     return _load().ep_oracle_validate(_ptr(idx), S, P, K, E, A, default_channels(S, C))
 
 
+def max_recv_rows(S: int, P: int, K: int) -> int:
+    """Worst-case receive rows over all destinations (the recv_src_idx size)."""
+    return int(_load().ep_oracle_max_recv_rows(S, P, K))
+
+
+def max_expanded_rows(S: int, P: int, K: int, E: int, A: int) -> int:
+    """Worst-case expanded rows, padding included (the exp_src size)."""
+    return int(_load().ep_oracle_max_expanded_rows(S, P, K, E, A))
+
+
 def plan(topk_idx: np.ndarray, S: int, P: int, E: int, A: int, C: int = 0) -> Plan:
     lib = _load()
     idx = np.ascontiguousarray(topk_idx, dtype=np.int64)

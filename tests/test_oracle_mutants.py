@@ -173,6 +173,22 @@ MUTANTS = [
      "recv_channel_prefix[((int64_t)s * P + d) * C + c] = base + in_src;"),
     ("fp8 input: codes of token 0",
      "out_q[r * H + h] = g >= 0 ? xq[(int64_t)g * H + h] : 0;", "out_q[r * H + h] = g >= 0 ? xq[h] : 0;"),
+    ("combine backward: weight gradient on an unused slot",
+     "grad_w[g * K + k] = dot;", "grad_w[g * K + k] = r >= 0 ? dot : 1.0;"),
+    ("bf16 round: NaN becomes infinity",
+     "return (uint16_t)((u >> 16) | 0x0040u);", "return (uint16_t)((u >> 16) & 0xff80u);"),
+    ("e4m3 decode: NaN code read as 480",
+     "if (exp_field == 0xf && mant == 7)", "if (exp_field == 0xf && mant == 8)"),
+    ("validate: channels beyond S accepted",
+     "K > E || (S > 0 && C > S)", "K > E || (S > 0 && C > S + 1)"),
+    ("worst expanded rows: padding term dropped",
+     "return (int64_t)P * S * K + (int64_t)E * (A - 1);", "return (int64_t)P * S * K;"),
+    ("worst receive rows: top-k not capped by P",
+     "return (int64_t)P * S * (K < P ? K : P);", "return (int64_t)P * S * K;"),
+    ("metadata: padding rows weigh 1",
+     "        recv_weights[r] = 0.0f;", "        recv_weights[r] = 1.0f;"),
+    ("channel ranges: last channel not clipped to S",
+     "if (hi > S) hi = S;", "if (hi > S + 1) hi = S + 1;"),
     ("fp8 input: scales of token 0",
      "out_scales[r * G + j] = g >= 0 ? xs[(int64_t)g * G + j] : 0.0f;",
      "out_scales[r * G + j] = g >= 0 ? xs[j] : 0.0f;"),

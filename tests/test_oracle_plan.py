@@ -266,6 +266,7 @@ def test_channels_equal_tokens():
 
 @pytest.mark.parametrize("mutate,kw", [
     ("range", {}), ("dup", {}), ("low", {}), (None, {"E": 9}), (None, {"A": 0}), (None, {"C": 100}),
+    (None, {"C": 65}),  # one channel more than the 64 tokens per rank
 ])
 def test_invalid_inputs(mutate, kw):
     w = WORKLOADS["tiny"]
@@ -280,6 +281,24 @@ def test_invalid_inputs(mutate, kw):
     assert oracle.validate(idx, w.S, w.P, E, A, C) == oracle.ERR_INVALID
     with pytest.raises(oracle.OracleError):
         oracle.plan(idx, w.S, w.P, E, A, C)
+
+
+@pytest.mark.parametrize("P,E,K", [(2, 8, 4), (4, 8, 2)])
+def test_receive_capacity_is_attained(P, E, K):
+    """Every token reaching min(K, P) ranks fills the receive windows to the
+    worst case T*min(K, P) the oracle sizes them for; random routing stays
+    below it."""
+    S, El = 8, E // P
+    # each token's K experts spread round-robin over the ranks
+    row = np.array([(k % P) * El + k // P for k in range(K)], np.int64)
+    idx = np.tile(row, (P * S, 1))
+    pl = oracle.plan(idx, S, P, E, A=1)
+    assert len(set(row // El)) == min(K, P)
+    assert pl.num_recv_total == oracle.max_recv_rows(S, P, K)
+    rng = np.random.default_rng(3)
+    idx = np.stack([rng.choice(E, K, replace=False) for _ in range(P * S)]).astype(np.int64)
+    pl = oracle.plan(idx, S, P, E, A=1)
+    assert pl.num_recv_total <= oracle.max_recv_rows(S, P, K)
 
 
 # ---------------------------------------------------------------------------
