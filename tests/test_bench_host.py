@@ -96,3 +96,17 @@ def test_reference_arm_prints_one_line_on_cpu():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_profile_summaries_name_their_command():
+    """Every committed ncu summary states the command that made it, and that
+    command runs committed files only."""
+    prof = os.path.join(ROOT, "profiles")
+    names = [n for n in os.listdir(prof) if n.endswith(".md")]
+    assert names
+    for n in names:
+        text = open(os.path.join(prof, n)).read()
+        cmds = [line for line in text.splitlines() if line.startswith("- command:")]
+        assert cmds, n
+        for line in cmds:
+            assert "_work/" not in line and "python bench.py" in line, (n, line)
