@@ -37,6 +37,8 @@
  *   - channel c of a source rank covers tokens [c*ceil(S/C), min(S,(c+1)*ceil(S/C)))
  *   - FP8: scale = amax/448 (fp32 IEEE division), q = E4M3_RNE_satfinite(x/scale);
  *     amax == 0 gives scale = 0 and all-zero codes
+ *   - FP8 on non-finite x: NaN elements are left out of amax, an infinite
+ *     element makes the scale +inf, and every NaN quotient encodes as 0x7f
  *   - combine: acc = 0.0f, then for k = 0..K-1 with slot >= 0:
  *     acc = fmaf(w[g,k], float(y[slot]), acc); out = bf16_RNE(acc)
  *
@@ -101,12 +103,16 @@ float ep_oracle_e4m3_to_f32(uint8_t b)
 /* Encode a binary32 value as E4M3 with round-to-nearest-even and saturation
  * of finite overflow to +-448.  Written from the format definition: find the
  * spacing of representable values in the binade of |v|, round |v|/spacing to
- * the nearest integer (ties to even), then lay the result out in fields. */
+ * the nearest integer (ties to even), then lay the result out in fields.
+ * Every NaN encodes as 0x7f (S.1111.111 with the sign bit clear): IEEE
+ * arithmetic leaves the sign of a NaN result unspecified (x86 and Arm hosts
+ * differ on inf/inf), so the reading fixes it, and the result does not
+ * depend on the CPU that computes the quotient. */
 uint8_t ep_oracle_f32_to_e4m3(float v)
 {
     uint8_t sign = signbit(v) ? 0x80 : 0x00;
     if (isnan(v))
-        return (uint8_t)(sign | 0x7f);
+        return (uint8_t)0x7f;
     if (isinf(v))
         return (uint8_t)(sign | 0x7e); /* satfinite: +-448 */
     double a = fabs((double)v);
@@ -359,7 +365,11 @@ void ep_oracle_dispatch_bf16(const uint16_t *x, int64_t H, const int32_t *exp_sr
 /* FP8 dispatch: for each expanded row and each group of 128 hidden elements,
  * amax = max |x| (exact in fp32), scale = amax / 448 (IEEE fp32 division),
  * q = E4M3(x / scale) with RNE and saturation; scales are row-major
- * [rows, H/128] fp32 ([TT] §3.6).  amax == 0 gives scale 0 and zero codes. */
+ * [rows, H/128] fp32 ([TT] §3.6).  amax == 0 gives scale 0 and zero codes.
+ * Non-finite x (the pages define none): NaN elements do not take part in
+ * amax (the comparison below is false for them); an infinite element makes
+ * amax and the scale +inf, so finite elements of its group give signed zero
+ * codes and the infinite one inf/inf = NaN; every NaN quotient is code 0x7f. */
 void ep_oracle_dispatch_fp8(const uint16_t *x, int64_t H, const int32_t *exp_src,
                             int64_t n_rows, int zero_pad, uint8_t *out_q,
                             float *out_scales)

@@ -34,6 +34,7 @@ PIN_FILES = [
     "test_oracle_dispatch_combine.py",
     "test_oracle_extras.py",
     "test_oracle_backward.py",
+    "test_oracle_nonfinite.py",
 ]
 
 # (name, text in ep_oracle.c (must occur once), replacement)
@@ -53,6 +54,11 @@ MUTANTS = [
      "        spacing = ldexp(1.0, -10);\n    } else {"),
     ("e4m3 encode: exponent bias 8",
      "int exp_field = (e2 - 1) + 7;", "int exp_field = (e2 - 1) + 8;"),
+    ("e4m3 encode: a NaN keeps its sign",
+     "        return (uint8_t)0x7f;", "        return (uint8_t)(sign | 0x7f);"),
+    ("fp8 amax: a NaN element takes over the group",
+     "                if (v > amax)\n                    amax = v;",
+     "                if (!(v <= amax))\n                    amax = v;"),
     ("e4m3 encode: infinity to NaN",
      "return (uint8_t)(sign | 0x7e); /* satfinite: +-448 */",
      "return (uint8_t)(sign | 0x7f); /* satfinite: +-448 */"),
