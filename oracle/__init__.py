@@ -7,9 +7,16 @@ baseline leg of the benchmark may import this package.  The product library
 The arithmetic lives in ``ep_oracle.c`` (plain C, compiled with gcc, no
 fast-math, no FP contraction).  This module only compiles it on demand,
 allocates numpy outputs and calls it through ctypes.
+
+The source is built twice: ``libep_oracle.so`` (single-threaded, the default)
+and ``libep_oracle_omp.so`` (the same source with ``-fopenmp``: the per-row
+loops of the scatter, combine and synthetic experts run on all host cores;
+every element is computed by the same code, so the bits are identical).
+``with oracle.parallel():`` routes calls to the multi-core build.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -25,6 +32,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.environ.get("EP_ORACLE_SOURCE") or os.path.join(_HERE, "ep_oracle.c")
 _LIB = (os.path.splitext(_SRC)[0] + ".so" if os.environ.get("EP_ORACLE_SOURCE")
         else os.path.join(_HERE, "libep_oracle.so"))
+# the multi-core build of the same source (not made for a modified copy)
+_LIB_OMP = None if os.environ.get("EP_ORACLE_SOURCE") else os.path.join(_HERE, "libep_oracle_omp.so")
+_CFLAGS = ["-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 
 OK = 0
 ERR_INVALID = 1
@@ -38,74 +48,123 @@ class OracleError(RuntimeError):
         self.code = code
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle source into its library next to it (atomic rename)."""
-    if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
-        return _LIB
-    fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(_LIB))
+def _compile(lib: str, extra) -> None:
+    if os.path.exists(lib) and os.path.getmtime(lib) >= os.path.getmtime(_SRC):
+        return
+    fd, tmp = tempfile.mkstemp(suffix=".so", dir=os.path.dirname(lib))
     os.close(fd)
-    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
-           "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    cmd = ["gcc", *_CFLAGS, *extra, "-o", tmp, _SRC, "-lm"]
     try:
         subprocess.run(cmd, check=True, capture_output=True, text=True)
-        os.replace(tmp, _LIB)
+        os.replace(tmp, lib)
     except subprocess.CalledProcessError as exc:  # pragma: no cover
         os.unlink(tmp)
         raise RuntimeError(f"oracle build failed:\n{exc.stderr}") from exc
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle source into its libraries next to it (atomic
+    renames): the single-threaded one, and the OpenMP one when gcc supports
+    -fopenmp.  Returns the single-threaded library's path."""
+    if force:
+        for lib in (_LIB, _LIB_OMP):
+            if lib and os.path.exists(lib):
+                os.unlink(lib)
+    _compile(_LIB, [])
+    if _LIB_OMP:
+        try:
+            _compile(_LIB_OMP, ["-fopenmp"])
+        except RuntimeError:  # pragma: no cover - a gcc without OpenMP
+            pass
     return _LIB
 
 
-_lib = None
+_libs = {}
+_use_omp = False
 
 
 def _load():
-    global _lib
-    if _lib is None:
-        lib = ctypes.CDLL(build())
-        P = ctypes.c_void_p
-        i64 = ctypes.c_int64
-        i32 = ctypes.c_int
-        lib.ep_oracle_validate.argtypes = [P, i64, i32, i32, i32, i32, i32]
-        lib.ep_oracle_validate.restype = i32
-        lib.ep_oracle_plan.argtypes = [P, i64, i32, i32, i32, i32, i32] + [P] * 11 + [i64, P, P, P, i64, P]
-        lib.ep_oracle_plan.restype = i32
-        lib.ep_oracle_dispatch_bf16.argtypes = [P, i64, P, i64, i32, P]
-        lib.ep_oracle_dispatch_bf16.restype = None
-        lib.ep_oracle_dispatch_fp8.argtypes = [P, i64, P, i64, i32, P, P]
-        lib.ep_oracle_dispatch_fp8.restype = None
-        lib.ep_oracle_combine.argtypes = [P, i64, P, P, i64, i32, P]
-        lib.ep_oracle_combine.restype = None
-        lib.ep_oracle_expert_scale.argtypes = [P, i64, P, P, i32, P]
-        lib.ep_oracle_expert_scale.restype = None
-        lib.ep_oracle_expert_scale_rows.argtypes = [P, i64, P, i64, i32, P]
-        lib.ep_oracle_expert_scale_rows.restype = None
-        lib.ep_oracle_combine_bias.argtypes = [P, i64, P, P, P, i64, i32, P]
-        lib.ep_oracle_combine_bias.restype = None
-        lib.ep_oracle_dispatch_metadata.argtypes = [P, P, i64, i32, i64, P, P]
-        lib.ep_oracle_dispatch_metadata.restype = None
-        lib.ep_oracle_dispatch_fp8_input.argtypes = [P, P, i64, P, i64, i32, P, P]
-        lib.ep_oracle_dispatch_fp8_input.restype = None
-        lib.ep_oracle_dispatch_backward.argtypes = [P, i64, P, i64, i32, P]
-        lib.ep_oracle_dispatch_backward.restype = None
-        lib.ep_oracle_combine_backward.argtypes = [P, P, i64, P, P, i64, P, i64, i32, i32, P, P]
-        lib.ep_oracle_combine_backward.restype = None
-        lib.ep_oracle_expert_dequant.argtypes = [P, P, i64, i64, P]
-        lib.ep_oracle_expert_dequant.restype = None
-        lib.ep_oracle_f32_to_bf16.argtypes = [ctypes.c_float]
-        lib.ep_oracle_f32_to_bf16.restype = ctypes.c_uint16
-        lib.ep_oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
-        lib.ep_oracle_bf16_to_f32.restype = ctypes.c_float
-        lib.ep_oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
-        lib.ep_oracle_f32_to_e4m3.restype = ctypes.c_uint8
-        lib.ep_oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
-        lib.ep_oracle_e4m3_to_f32.restype = ctypes.c_float
-        lib.ep_oracle_max_recv_rows.argtypes = [i64, i32, i32]
-        lib.ep_oracle_max_recv_rows.restype = i64
-        lib.ep_oracle_max_expanded_rows.argtypes = [i64, i32, i32, i32, i32]
-        lib.ep_oracle_max_expanded_rows.restype = i64
-        _lib = lib
-    return _lib
+    """The active library: the OpenMP build inside ``parallel()``, else the
+    single-threaded one."""
+    omp = _use_omp and _LIB_OMP is not None
+    if omp not in _libs:
+        build()
+        if omp:
+            if not os.path.exists(_LIB_OMP):
+                raise RuntimeError("the OpenMP build of the oracle is unavailable (gcc without -fopenmp)")
+            # idle worker threads sleep instead of spinning between calls
+            os.environ.setdefault("OMP_WAIT_POLICY", "PASSIVE")
+        _libs[omp] = _setup(ctypes.CDLL(_LIB_OMP if omp else _LIB))
+    return _libs[omp]
+
+
+@contextlib.contextmanager
+def parallel(enabled: bool = True):
+    """Route oracle calls in this block to the OpenMP build (all host cores)."""
+    global _use_omp
+    old = _use_omp
+    _use_omp = bool(enabled)
+    try:
+        yield
+    finally:
+        _use_omp = old
+
+
+def threads() -> int:
+    """Threads the active build's row loops use (1 for the plain build)."""
+    return int(_load().ep_oracle_threads())
+
+
+def omp_available() -> bool:
+    build()
+    return _LIB_OMP is not None and os.path.exists(_LIB_OMP)
+
+
+def _setup(lib):
+    P = ctypes.c_void_p
+    i64 = ctypes.c_int64
+    i32 = ctypes.c_int
+    lib.ep_oracle_validate.argtypes = [P, i64, i32, i32, i32, i32, i32]
+    lib.ep_oracle_validate.restype = i32
+    lib.ep_oracle_plan.argtypes = [P, i64, i32, i32, i32, i32, i32] + [P] * 11 + [i64, P, P, P, i64, P]
+    lib.ep_oracle_plan.restype = i32
+    lib.ep_oracle_dispatch_bf16.argtypes = [P, i64, P, i64, i32, P]
+    lib.ep_oracle_dispatch_bf16.restype = None
+    lib.ep_oracle_dispatch_fp8.argtypes = [P, i64, P, i64, i32, P, P]
+    lib.ep_oracle_dispatch_fp8.restype = None
+    lib.ep_oracle_combine.argtypes = [P, i64, P, P, i64, i32, P]
+    lib.ep_oracle_combine.restype = None
+    lib.ep_oracle_expert_scale.argtypes = [P, i64, P, P, i32, P]
+    lib.ep_oracle_expert_scale.restype = None
+    lib.ep_oracle_expert_scale_rows.argtypes = [P, i64, P, i64, i32, P]
+    lib.ep_oracle_expert_scale_rows.restype = None
+    lib.ep_oracle_combine_bias.argtypes = [P, i64, P, P, P, i64, i32, P]
+    lib.ep_oracle_combine_bias.restype = None
+    lib.ep_oracle_dispatch_metadata.argtypes = [P, P, i64, i32, i64, P, P]
+    lib.ep_oracle_dispatch_metadata.restype = None
+    lib.ep_oracle_dispatch_fp8_input.argtypes = [P, P, i64, P, i64, i32, P, P]
+    lib.ep_oracle_dispatch_fp8_input.restype = None
+    lib.ep_oracle_dispatch_backward.argtypes = [P, i64, P, i64, i32, P]
+    lib.ep_oracle_dispatch_backward.restype = None
+    lib.ep_oracle_combine_backward.argtypes = [P, P, i64, P, P, i64, P, i64, i32, i32, P, P]
+    lib.ep_oracle_combine_backward.restype = None
+    lib.ep_oracle_expert_dequant.argtypes = [P, P, i64, i64, P]
+    lib.ep_oracle_expert_dequant.restype = None
+    lib.ep_oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.ep_oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.ep_oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.ep_oracle_bf16_to_f32.restype = ctypes.c_float
+    lib.ep_oracle_f32_to_e4m3.argtypes = [ctypes.c_float]
+    lib.ep_oracle_f32_to_e4m3.restype = ctypes.c_uint8
+    lib.ep_oracle_e4m3_to_f32.argtypes = [ctypes.c_uint8]
+    lib.ep_oracle_e4m3_to_f32.restype = ctypes.c_float
+    lib.ep_oracle_max_recv_rows.argtypes = [i64, i32, i32]
+    lib.ep_oracle_max_recv_rows.restype = i64
+    lib.ep_oracle_max_expanded_rows.argtypes = [i64, i32, i32, i32, i32]
+    lib.ep_oracle_max_expanded_rows.restype = i64
+    lib.ep_oracle_threads.argtypes = []
+    lib.ep_oracle_threads.restype = i32
+    return lib
 
 
 def _ptr(a: np.ndarray) -> int:

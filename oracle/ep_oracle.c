@@ -43,15 +43,34 @@
  *     acc = fmaf(w[g,k], float(y[slot]), acc); out = bf16_RNE(acc)
  *
  * Compile: gcc -O2 -std=c11 -ffp-contract=off -fPIC -shared (no fast-math).
+ * The same source built with -fopenmp is the multi-core variant: the
+ * "omp parallel for" lines below split the per-row loops of the scatter, the
+ * combine and the synthetic experts over threads.  Every output element is
+ * still computed by the same sequential code in the same order; only which
+ * thread computes which rows changes, so both builds give identical bits.
+ * Without -fopenmp the pragmas are ignored.  The plan stays sequential.
  */
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define ORACLE_OK 0
 #define ORACLE_ERR_INVALID 1
 #define ORACLE_ERR_CAPACITY 2
+
+/* Threads the row loops use: 1 for the plain build. */
+int ep_oracle_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------------ */
 /* Number formats                                                            */
@@ -351,6 +370,7 @@ int ep_oracle_plan(const int64_t *topk_idx, int64_t S, int P, int K, int E, int 
 void ep_oracle_dispatch_bf16(const uint16_t *x, int64_t H, const int32_t *exp_src,
                              int64_t n_rows, int zero_pad, uint16_t *out)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n_rows; ++r) {
         int32_t g = exp_src[r];
         for (int64_t h = 0; h < H; ++h) {
@@ -375,6 +395,7 @@ void ep_oracle_dispatch_fp8(const uint16_t *x, int64_t H, const int32_t *exp_src
                             float *out_scales)
 {
     const int64_t G = H / 128;
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n_rows; ++r) {
         int32_t g = exp_src[r];
         if (g < 0) {
@@ -420,6 +441,7 @@ void ep_oracle_combine_bias(const uint16_t *y, int64_t H, const int32_t *slot,
                             const float *topk_weights, const uint16_t *bias, int64_t T, int K,
                             uint16_t *out)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t g = 0; g < T; ++g)
         for (int64_t h = 0; h < H; ++h) {
             float acc = 0.0f;
@@ -438,6 +460,7 @@ void ep_oracle_combine_bias(const uint16_t *y, int64_t H, const int32_t *slot,
 void ep_oracle_combine(const uint16_t *y, int64_t H, const int32_t *slot,
                        const float *topk_weights, int64_t T, int K, uint16_t *out)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t g = 0; g < T; ++g)
         for (int64_t h = 0; h < H; ++h) {
             float acc = 0.0f;
@@ -462,6 +485,7 @@ void ep_oracle_expert_scale(const uint16_t *x_exp, int64_t H, const int32_t *exp
 {
     for (int e = 0; e < E; ++e) {
         float f = 1.0f + (float)e / (float)E;
+#pragma omp parallel for schedule(static)
         for (int64_t r = expert_offsets[e]; r < expert_offsets[e + 1]; ++r)
             for (int64_t h = 0; h < H; ++h)
                 y[r * H + h] = exp_src[r] >= 0
@@ -475,6 +499,7 @@ void ep_oracle_expert_dequant(const uint8_t *q, const float *scales, int64_t H,
                               int64_t n_rows, uint16_t *y)
 {
     const int64_t G = H / 128;
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n_rows; ++r)
         for (int64_t h = 0; h < H; ++h)
             y[r * H + h] = ep_oracle_f32_to_bf16(ep_oracle_e4m3_to_f32(q[r * H + h]) * scales[r * G + h / 128]);
@@ -485,6 +510,7 @@ void ep_oracle_expert_dequant(const uint8_t *q, const float *scales, int64_t H,
 void ep_oracle_expert_scale_rows(const uint16_t *x_rows, int64_t H, const int32_t *row_expert,
                                  int64_t n_rows, int E, uint16_t *y)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n_rows; ++r) {
         int e = row_expert[r];
         float f = e >= 0 ? 1.0f + (float)e / (float)E : 0.0f;
@@ -507,6 +533,7 @@ void ep_oracle_expert_scale_rows(const uint16_t *x_rows, int64_t H, const int32_
 void ep_oracle_dispatch_backward(const uint16_t *grad_recv, int64_t H, const int32_t *slot,
                                  int64_t T, int K, uint16_t *grad_x)
 {
+#pragma omp parallel for schedule(static)
     for (int64_t g = 0; g < T; ++g)
         for (int64_t h = 0; h < H; ++h) {
             float acc = 0.0f;
@@ -584,6 +611,7 @@ void ep_oracle_dispatch_fp8_input(const uint8_t *xq, const float *xs, int64_t H,
                                   int64_t n_rows, int zero_pad, uint8_t *out_q, float *out_scales)
 {
     const int64_t G = H / 128;
+#pragma omp parallel for schedule(static)
     for (int64_t r = 0; r < n_rows; ++r) {
         int32_t g = exp_src[r];
         if (g < 0 && !zero_pad)

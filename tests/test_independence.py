@@ -52,9 +52,11 @@ def test_cuda_sources_reference_no_oracle_file():
 def test_oracle_uses_only_standard_headers_and_numpy():
     src = open(os.path.join(ORACLE, "ep_oracle.c")).read()
     includes = re.findall(r'^\s*#\s*include\s*[<"]([^>"]+)[>"]', src, re.M)
-    assert includes and set(includes) <= {"math.h", "stdint.h", "stdlib.h", "string.h"}, includes
+    # omp.h: the compiler's OpenMP runtime, for the multi-core build of the same source
+    assert includes and set(includes) <= {"math.h", "stdint.h", "stdlib.h", "string.h", "omp.h"}, includes
     mods = set(_imports(os.path.join(ORACLE, "__init__.py")))
-    assert mods <= {"__future__", "ctypes", "os", "subprocess", "tempfile", "dataclasses", "numpy"}, mods
+    assert mods <= {"__future__", "contextlib", "ctypes", "os", "subprocess", "tempfile", "dataclasses",
+                    "numpy"}, mods
 
 
 def test_input_generators_do_no_method_arithmetic():

@@ -135,10 +135,12 @@ MUTANTS = [
     ("combine: last slot dropped",
      "void ep_oracle_combine(const uint16_t *y, int64_t H, const int32_t *slot,\n"
      "                       const float *topk_weights, int64_t T, int K, uint16_t *out)\n{\n"
+     "#pragma omp parallel for schedule(static)\n"
      "    for (int64_t g = 0; g < T; ++g)\n        for (int64_t h = 0; h < H; ++h) {\n"
      "            float acc = 0.0f;\n            for (int k = 0; k < K; ++k) {",
      "void ep_oracle_combine(const uint16_t *y, int64_t H, const int32_t *slot,\n"
      "                       const float *topk_weights, int64_t T, int K, uint16_t *out)\n{\n"
+     "#pragma omp parallel for schedule(static)\n"
      "    for (int64_t g = 0; g < T; ++g)\n        for (int64_t h = 0; h < H; ++h) {\n"
      "            float acc = 0.0f;\n            for (int k = 0; k < K - 1; ++k) {"),
     ("combine: weights ignored",
@@ -148,8 +150,8 @@ MUTANTS = [
      "            }\n            out[g * H + h]"),
     # --- synthetic experts ---
     ("scaling expert: factor 1 + e/(E-1)",
-     "        float f = 1.0f + (float)e / (float)E;\n        for (int64_t r = expert_offsets[e]",
-     "        float f = 1.0f + (float)e / (float)(E - 1);\n        for (int64_t r = expert_offsets[e]"),
+     "        float f = 1.0f + (float)e / (float)E;\n#pragma omp parallel for",
+     "        float f = 1.0f + (float)e / (float)(E - 1);\n#pragma omp parallel for"),
     ("dequant expert: scale of the next group",
      "scales[r * G + h / 128]", "scales[r * G + (h / 128 + 1) % G]"),
     # --- backward ---
