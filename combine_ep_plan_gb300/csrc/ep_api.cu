@@ -189,6 +189,9 @@ size_t layout_handle(ep_handle_s* h, char* base) {
   const size_t o_esrc = L.take(sizeof(int) * h->cap_exp);
   h->cap_pad = E * (A - 1);
   const size_t o_pads = L.take(sizeof(int) * (h->cap_pad > 0 ? h->cap_pad : 1));
+  p.cap_recv = h->cap_recv;
+  p.cap_exp = h->cap_exp;
+  p.cap_pad = h->cap_pad;
   const size_t o_inr = L.take(sizeof(unsigned char) * T * P);
   const size_t total = L.take(0);
   if (base) {

@@ -144,10 +144,16 @@ int resident_grid(Kernel kernel, int threads) {
 
 template <int KMAX, int U, int MINB, bool PROF>
 cudaError_t launch_kp(const CombineDev& c, cudaStream_t stream, const LaunchCfg& cfg) {
-  thread_local int full = 0;  // per host thread; one device type per process
+  // one resident wave, cached per host thread for the last device it was
+  // asked for
+  thread_local int full = 0, full_dev = -1;
   auto kernel = ep_combine_kernel<KMAX, U, MINB, PROF>;
-  if (full == 0)
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  if (full == 0 || dev != full_dev) {
     full = EP_COMBINE_CTAS_PER_SM > 0 ? EP_COMBINE_CTAS_PER_SM * num_sms() : resident_grid(kernel, 256);
+    full_dev = dev;
+  }
   long long grid = full;
   const long long cap = budget_cap(kernel, 256, 0, cfg.sm_budget);
   if (cap > 0 && grid > cap) grid = cap;
@@ -178,9 +184,9 @@ __device__ __forceinline__ void combine_backward_item(const CombineBwdDev& c, in
   uint4* gy = static_cast<uint4*>(c.grad_y);
   if (item >= c.T) {
     const int64_t pi = item - c.T;
-    if (pi >= c.sizes[kSizePad]) return;
+    if (pi >= c.sizes[kSizePad] || pi >= c.max_pad) return;
     const int r = c.pad_rows[pi];
-    if (r >= c.grad_y_rows) {
+    if (r < 0 || r >= c.grad_y_rows) {
       if (threadIdx.x == 0) atomicOr(c.status, kStCapacity);
       return;
     }

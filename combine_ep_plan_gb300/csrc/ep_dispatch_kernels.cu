@@ -32,6 +32,12 @@ __device__ __forceinline__ void st_row(uint4* p, const uint4& v) {
 // Unroll factor: 16-byte vectors per lane loaded before the K stores.
 constexpr int kUnroll = 4;
 
+// N_pad as the plan wrote it, at most max_pad (the entries the handle holds).
+__device__ __forceinline__ int64_t pad_count(const DispatchDev& a) {
+  const int64_t n = a.sizes[kSizePad];
+  return n < a.max_pad ? n : a.max_pad;
+}
+
 // Work item = (row item, column chunk of 32*kUnroll vectors): T token rows
 // then N_pad padding rows, each cut into chunks, so that every warp gets many
 // small items and the kernel has no long tail.
@@ -73,7 +79,7 @@ __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
   const int64_t groups = a.H / 128;
   constexpr int kChunk = 32 * kUnroll;
   const int64_t chunks = (hv + kChunk - 1) / kChunk;
-  const int64_t n_pad = a.zero_pad ? a.sizes[kSizePad] : 0;
+  const int64_t n_pad = a.zero_pad ? pad_count(a) : 0;
   const int64_t n_items = (a.T + n_pad) * chunks;
   const uint4* x = static_cast<const uint4*>(a.x);
   uint4* out = static_cast<uint4*>(a.out);
@@ -118,7 +124,7 @@ __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
       }
     } else {
       const int r = a.pad_rows[ri - a.T];
-      if (r >= a.capacity) {
+      if (r < 0 || r >= a.capacity) {
         if (lane == 0) atomicOr(a.status, kStCapacity);
         continue;
       }
@@ -217,7 +223,7 @@ __global__ void __launch_bounds__(kFp8Cta, PROF ? 768 / kFp8Cta : 1024 / kFp8Cta
   constexpr int kUnitVec = 32;                 // 16-element units per warp per unit step
   constexpr int kChunkVec = kUnitVec * kFp8Units;
   const int64_t chunks = (qv + kChunkVec - 1) / kChunkVec;
-  const int64_t n_pad = a.zero_pad ? a.sizes[kSizePad] : 0;
+  const int64_t n_pad = a.zero_pad ? pad_count(a) : 0;
   const int64_t n_items = (a.T + n_pad) * chunks;
   const uint4* x = static_cast<const uint4*>(a.x);
   uint4* out = static_cast<uint4*>(a.out);
@@ -329,7 +335,7 @@ __global__ void __launch_bounds__(kFp8Cta, PROF ? 768 / kFp8Cta : 1024 / kFp8Cta
       }
     } else {
       const int r = a.pad_rows[ri - a.T];
-      if (r >= a.capacity) {
+      if (r < 0 || r >= a.capacity) {
         if (lane == 0) atomicOr(a.status, kStCapacity);
         continue;
       }
@@ -405,9 +411,9 @@ __global__ void __launch_bounds__(256) ep_dispatch_metadata_kernel(MetaDev m) {
     return;
   }
   const int64_t pi = i - pairs;
-  if (pi >= m.sizes[kSizePad]) return;
+  if (pi >= m.sizes[kSizePad] || pi >= m.max_pad) return;
   const int r = m.pad_rows[pi];
-  if (r >= m.capacity) {
+  if (r < 0 || r >= m.capacity) {
     atomicOr(m.status, kStCapacity);
     return;
   }

@@ -25,7 +25,11 @@ constexpr unsigned kStTimeout = 8u;     // a bounded grid-barrier wait gave up
 // parity of a generation word every CTA reads when the plan starts; after
 // the second barrier CTA 0 zeroes the other count and bumps the generation,
 // so each launch (and each replay of a captured launch) finds a zeroed count
-// and leaves one for the next.
+// and leaves one for the next.  A launch whose barrier wait gave up leaves
+// its count as it was and sets kStTimeout; until the host clears the control
+// words (when it reads the status), later launches that find kStTimeout set
+// do not arrive at a barrier at all, so that no launch can pass a barrier on
+// a timed-out launch's arrivals.
 constexpr int kCtrBarCount = 0;   // grid barriers: CTAs arrived, generation 0, 2, ...
 constexpr int kCtrBarCount1 = 32; // ... generation 1, 3, ...
 constexpr int kCtrBarGen = 64;    // generation
@@ -189,6 +193,10 @@ struct PlanDev {
   int* exp_src;        // [T*K + E*(A-1)]
   int* pad_rows;       // [E*(A-1)]
   unsigned char* in_rank;  // [T,P]
+  // entries allocated in recv_src_idx, exp_src and pad_rows: every store the
+  // plan makes at an index derived from other CTAs' counts is checked
+  // against them (an index beyond records kStCapacity and is not written)
+  int64_t cap_recv, cap_exp, cap_pad;
   // bounded wait of the grid barriers, and a test hook (a tile whose CTA
   // returns before the first barrier)
   long long poll_limit;

@@ -99,8 +99,10 @@ __device__ __forceinline__ void build_tile_bits(const PlanDev& p, const int* ids
 // arrival to this launch's count (a release reduction: nothing to wait for)
 // and polls it until it reaches `round` times the grid: the release of the
 // last CTA is the one reduction, seen by each poller one load later.
-// `count` is meaningful in thread 0 only.
-__device__ bool grid_sync(const PlanDev& p, unsigned* count, unsigned round) {
+// `count` and `refuse` are meaningful in thread 0 only; a CTA that refuses
+// (the launch found a timed-out predecessor's mark) neither arrives nor
+// waits, and fails the barrier.
+__device__ bool grid_sync(const PlanDev& p, unsigned* count, unsigned round, bool refuse) {
   __shared__ int s_ok;
   if (gridDim.x == 1) {  // a one-CTA plan: the CTA barrier orders everything
     __syncthreads();
@@ -108,23 +110,31 @@ __device__ bool grid_sync(const PlanDev& p, unsigned* count, unsigned round) {
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    const unsigned target = round * gridDim.x;
-    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
-    int ok = 1;
-    long long polls = 0;
-    unsigned ns = 32;
-    while (static_cast<int>(ld_acquire(count) - target) < 0) {
-      if (++polls > p.poll_limit) {
-        ok = 0;
-        break;
+    int ok = 0;
+    if (!refuse) {
+      const unsigned target = round * gridDim.x;
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(count) : "memory");
+      ok = 1;
+      long long polls = 0;
+      unsigned ns = 32;
+      while (static_cast<int>(ld_acquire(count) - target) < 0) {
+        if (++polls > p.poll_limit) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(ns);
+        if (ns < 128) ns <<= 1;
       }
-      __nanosleep(ns);
-      if (ns < 128) ns <<= 1;
     }
     s_ok = ok;
   }
   __syncthreads();
   return s_ok != 0;
+}
+
+// i < n for a signed index and a capacity, as one unsigned comparison.
+__device__ __forceinline__ bool in_cap(int64_t i, int64_t n) {
+  return static_cast<uint64_t>(i) < static_cast<uint64_t>(n);
 }
 
 // Column scans, one warp per column: the tiles' counts in order, 32 at a
@@ -277,8 +287,10 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
   extern __shared__ __align__(16) uint32_t smem[];
   unsigned long long t_start = 0, t_scan = 0, t_bar1 = 0, t_bar2 = 0, scanned = 0;
   if (PROF && threadIdx.x == 0) t_start = prof_now();
-  // this launch's barrier count (thread 0; the read is first used at barrier 1)
+  // this launch's barrier count, and whether a launch before it timed out
+  // (thread 0; both reads are first used at barrier 1)
   const unsigned gen = threadIdx.x == 0 ? __ldcg(&p.ctr[kCtrBarGen]) : 0u;
+  const unsigned status0 = threadIdx.x == 0 ? __ldcg(&p.ctr[kCtrStatus]) : 0u;
   unsigned* bar_count = p.ctr + ((gen & 1u) ? kCtrBarCount1 : kCtrBarCount);
 
   // ---------------- phase 1: tiles ----------------
@@ -314,13 +326,13 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
     __syncthreads();  // before the next tile reuses shared memory (and for phase 2)
   }
 
-  if (!grid_sync(p, bar_count, 1)) {
+  if (!grid_sync(p, bar_count, 1, (status0 & kStTimeout) != 0)) {
     if (threadIdx.x == 0) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
     return;
   }
   if (PROF && threadIdx.x == 0) t_bar1 = prof_now();
   column_scans(p);
-  if (!grid_sync(p, bar_count, 2)) {
+  if (!grid_sync(p, bar_count, 2, false)) {
     if (threadIdx.x == 0) atomicOr(&p.ctr[kCtrStatus], kStTimeout);
     return;
   }
@@ -389,7 +401,12 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
           int r = -1;
           if (e >= 0) {
             r = exp_off[e] + tile_pos(bits, s_run, p.ncols, p.P + e, i);
-            p.exp_src[r] = static_cast<int>(t0 + i);
+            if (in_cap(r, p.cap_exp)) {
+              p.exp_src[r] = static_cast<int>(t0 + i);
+            } else {
+              atomicOr(&p.ctr[kCtrStatus], kStCapacity);
+              r = -1;
+            }
           }
           s_slot[i * p.K + k] = r;
         }
@@ -429,7 +446,12 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
         int r = -1;
         if (e[k] >= 0) {
           r = exp_off[e[k]] + pre[k] + __popc(bw[k] & below);
-          p.exp_src[r] = static_cast<int>(g);
+          if (in_cap(r, p.cap_exp)) {
+            p.exp_src[r] = static_cast<int>(g);
+          } else {
+            atomicOr(&p.ctr[kCtrStatus], kStCapacity);
+            r = -1;
+          }
         }
         p.slot[g * p.K + k] = r;
       }
@@ -471,7 +493,13 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
           const int bit = (word >> (l0 + l)) & 1;
           p.in_rank[g * p.P + d] = static_cast<unsigned char>(bit);
           p.send_head[g * p.P + d] = bit ? pos : -1;
-          if (bit) p.recv_src_idx[base + pos++] = t_local;
+          if (bit) {
+            const int64_t at_r = static_cast<int64_t>(base) + pos++;
+            if (in_cap(at_r, p.cap_recv))
+              p.recv_src_idx[at_r] = t_local;
+            else
+              atomicOr(&p.ctr[kCtrStatus], kStCapacity);
+          }
           if (++t_local == p.S) t_local = 0;
         }
       }
@@ -510,7 +538,9 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
   }
 
   // padding rows of the expanded layout
-  for (int64_t i = small_passes ? (stid + snthr / 4) % snthr : INT64_MAX; i < n_pad; i += snthr) {
+  const int64_t n_pad_w = n_pad < p.cap_pad ? n_pad : p.cap_pad;
+  if (small_passes && stid == 0 && n_pad > p.cap_pad) atomicOr(&p.ctr[kCtrStatus], kStCapacity);
+  for (int64_t i = small_passes ? (stid + snthr / 4) % snthr : INT64_MAX; i < n_pad_w; i += snthr) {
     int lo = 0, hi = p.E;  // e with pad_off[e] <= i < pad_off[e+1]
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
@@ -520,7 +550,10 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
     const int n_e = (exp_off[e + 1] - exp_off[e]) - (pad_off[e + 1] - pad_off[e]);
     const int row = exp_off[e] + n_e + static_cast<int>(i - pad_off[e]);
     p.pad_rows[i] = row;
-    p.exp_src[row] = -1;
+    if (in_cap(row, p.cap_exp))
+      p.exp_src[row] = -1;
+    else
+      atomicOr(&p.ctr[kCtrStatus], kStCapacity);
   }
   if (PROF) prof_cta_end(p, kProfPlan, t_start, t_scan, t_bar1, t_bar2, scanned, 0);
 }
@@ -548,16 +581,21 @@ namespace {
 template <bool PROF, int KMAX>
 int plan_grid(const PlanDev& p, int sm_budget) {
   const size_t smem = plan_smem_bytes(p.P, p.E, p.K);
-  // occupancy per host thread (one device type per process)
+  // occupancy, cached per host thread for the last (device, shared memory)
+  // it was asked for
+  thread_local int cached_dev = -1;
   thread_local size_t cached_smem = ~static_cast<size_t>(0);
   thread_local int cached_per_sm = 0;
-  if (smem != cached_smem) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (smem != cached_smem || dev != cached_dev) {
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ep_plan_kernel<PROF, KMAX>, kTile, smem) != cudaSuccess ||
         per_sm < 1)
       return 0;
     cached_per_sm = per_sm > kPlanThreadsPerSm / kTile ? kPlanThreadsPerSm / kTile : per_sm;
     cached_smem = smem;
+    cached_dev = dev;
   }
   const int sms = sm_budget > 0 && sm_budget < num_sms() ? sm_budget : num_sms();
   const int64_t cap = static_cast<int64_t>(cached_per_sm) * sms;

@@ -1,14 +1,15 @@
 // ep_static_scratch.cu — ep_plan_static_scratch: the routing plan for callers
 // that cannot allocate device memory.
 //
-// ep_plan keeps its plan arrays and its scratch (per-tile counts and prefixes, tile
-// ticket, done counter, status word, column totals) in one allocation that it
-// makes per handle.  Some callers cannot allocate at that point: a serving
+// ep_plan keeps its plan arrays and its scratch (per-tile counts and
+// prefixes, tile bit matrices, barrier counts, status word, column totals) in
+// one allocation that it makes per handle.  Some callers cannot allocate at that point: a serving
 // runtime that reserved all device memory for its own arena at start-up, or a
 // latency-critical loop where an allocation may block on the device or fail
 // under fragmentation.  This entry point runs the same plan kernels, writes
 // the plan into arrays the caller owns, and keeps its scratch in a fixed
 // file-scope device array instead.
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -24,25 +25,39 @@ __device__ __align__(256) unsigned char g_plan_scratch[EP_STATIC_SCRATCH_BYTES];
 constexpr int kMaxDevices = 64;
 
 struct DeviceScratch {
-  std::once_flag once;
-  void* ptr = nullptr;
-  cudaError_t err = cudaSuccess;
+  std::mutex mu;
+  std::atomic<void*> ptr{nullptr};
 };
 DeviceScratch g_scratch[kMaxDevices];
 
 // Device address of g_plan_scratch on the current device.  In host code the
 // array's name only stands in for the symbol; the address a kernel may use
-// comes from cudaGetSymbolAddress, looked up once per device with that device
-// current (on the first call of the entry point on it).
+// comes from cudaGetSymbolAddress, looked up with that device current on the
+// first successful call of the entry point on it and kept from then on.  A
+// failed lookup is not kept: the next call tries again (and the runtime's
+// last-error slot is cleared, so that it does not surface in a later,
+// unrelated launch check).
 cudaError_t scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   DeviceScratch& s = g_scratch[dev];
-  std::call_once(s.once, [&s] { s.err = cudaGetSymbolAddress(&s.ptr, g_plan_scratch); });
-  *out = s.ptr;
-  return s.err;
+  void* p = s.ptr.load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(s.mu);
+    p = s.ptr.load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      e = cudaGetSymbolAddress(&p, g_plan_scratch);
+      if (e != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
+        return e != cudaSuccess ? e : cudaErrorInvalidSymbol;
+      }
+      s.ptr.store(p, std::memory_order_release);
+    }
+  }
+  *out = p;
+  return cudaSuccess;
 }
 
 size_t round256(size_t n) { return (n + 255) & ~static_cast<size_t>(255); }
@@ -136,6 +151,9 @@ extern "C" ep_status_t ep_plan_static_scratch(const int64_t* topk_idx, int64_t S
   p.exp_src = out->exp_src;
   p.pad_rows = out->pad_rows;
   p.in_rank = out->is_token_in_rank;
+  p.cap_recv = T * (K < P ? K : P);
+  p.cap_exp = T * K + static_cast<int64_t>(E) * (A - 1);
+  p.cap_pad = static_cast<int64_t>(E) * (A - 1);
   p.poll_limit = 1ll << 20;
   p.suppress_tile = -1;
 

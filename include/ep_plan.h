@@ -19,6 +19,13 @@
  *     capacity, a bounded wait that gave up) are recorded in the handle's
  *     device status word; no out-of-range row is ever written.  They are
  *     returned by the next synchronising call (ep_plan_sizes, ep_sync_status).
+ *   - A plan whose bounded wait gave up (EP_ERR_TIMEOUT) leaves the handle's
+ *     plan arrays unfinished.  Until ep_sync_status reads and clears that
+ *     status, later plans on the handle do no work (they could otherwise
+ *     pass a grid barrier on the timed-out plan's arrivals), and dispatch,
+ *     combine and backward calls on the handle keep every access inside the
+ *     caller's buffers and the handle's arrays but produce unspecified rows.
+ *     ep_plan_sizes and ep_pending_wait report the status without clearing it.
  *   - A handle is not thread-safe; calls that use one handle on different
  *     streams must be ordered by the caller.
  *   - ep_replan, ep_dispatch, ep_dispatch_cached, ep_dispatch_metadata,
@@ -296,7 +303,9 @@ ep_status_t ep_combine_backward(ep_handle_t handle, const void *grad_out_dev, co
 
 /*
  * ep_sync_status — synchronises `stream`, returns the first error recorded in
- * the handle's device status word (EP_OK if none) and clears it.
+ * the handle's device status word (EP_OK if none) and clears it; after
+ * EP_ERR_TIMEOUT it also resets the plan's grid-barrier words, so that the
+ * next plan runs normally.
  */
 ep_status_t ep_sync_status(ep_handle_t handle, ep_stream_t stream);
 
@@ -343,8 +352,12 @@ ep_status_t ep_handle_destroy(ep_handle_t handle, ep_stream_t stream);
  * device-to-device copies on `stream`.
  *
  * - The first call on a device looks up the scratch array's device address
- *   (cudaGetSymbolAddress, with that device current); make that first call
- *   before any stream capture.
+ *   (cudaGetSymbolAddress, with that device current).  Under CUDA's lazy
+ *   module loading (the default) that lookup is also where the library's
+ *   device code, and with it the scratch array, is loaded onto the device:
+ *   "allocates nothing" holds from the first successful call on.  Make that
+ *   first call before any stream capture.  A failed lookup is not kept: the
+ *   next call tries again.
  * - All calls on a device share the one scratch array, and it keeps the last
  *   call's contents; each call clears what it needs.  Calls whose work
  *   overlaps on the GPU (other streams, other threads) race on the scratch:
@@ -357,8 +370,9 @@ ep_status_t ep_handle_destroy(ep_handle_t handle, ep_stream_t stream);
  * - Arguments and shape limits are those of ep_plan; out and all its pointers
  *   must be non-NULL device pointers, 4-byte aligned except the uint8 array.
  *   out->info receives {N_recv, N_exp, N_pad, device status bits}; status
- *   bit 1 = expert id out of range, 2 = duplicate expert in a row, 8 = a
- *   bounded wait gave up (the plan is then invalid).
+ *   bit 1 = expert id out of range, 2 = duplicate expert in a row, 4 = an
+ *   index beyond the buffers' sizes (not written; only after a failed wait),
+ *   8 = a bounded wait gave up (the plan is then invalid).
  */
 #define EP_STATIC_SCRATCH_BYTES (4u << 20)
 

@@ -56,3 +56,26 @@ def u16(t: torch.Tensor) -> np.ndarray:
 
 def u8(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.uint8).numpy()
+
+
+_BYTES = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64}
+
+
+def assert_bits_equal(got: torch.Tensor, want: np.ndarray, name: str = "array"):
+    """Bit-for-bit equality of a device tensor with an oracle array, compared
+    on the device (whole arrays at full size); on a mismatch, the count and
+    the first positions."""
+    want = np.ascontiguousarray(want)
+    assert tuple(got.shape) == want.shape, f"{name}: shape {tuple(got.shape)} != oracle {want.shape}"
+    if got.numel() == 0:
+        return
+    dt = _BYTES[want.dtype.itemsize]
+    assert got.element_size() == want.dtype.itemsize, f"{name}: element size differs"
+    g = got.contiguous().view(dt)
+    w = torch.from_numpy(want.view(np.dtype(str(dt).replace("torch.", "")))).to(got.device)
+    if torch.equal(g, w):
+        return
+    bad = torch.nonzero(g != w)
+    first = bad[:5].cpu().tolist()
+    raise AssertionError(f"{name}: {bad.shape[0]} of {g.numel()} elements differ, first at {first}: "
+                         f"gpu {[int(g[tuple(i)]) for i in first]} oracle {[int(w[tuple(i)]) for i in first]}")

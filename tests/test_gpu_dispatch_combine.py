@@ -1,7 +1,7 @@
 """GPU parity of dispatch (BF16 bit copy, FP8 E4M3 quantised inside dispatch)
-and combine, against the oracle: element by element on cases that span
-several tiles with a ragged tail, and on sampled rows/tokens at the full
-workload sizes in the launch configuration the benchmark uses."""
+and combine, against the oracle, element by element: on cases that span
+several tiles with a ragged tail, and on whole arrays at the full workload
+sizes in the launch configuration the benchmark uses."""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +10,7 @@ import combine_ep_plan_gb300 as ep
 import oracle
 from combine_ep_plan_gb300.inputs import (WORKLOADS, bits_to_bf16_tensor, draw_hidden, draw_topk, draw_y,
                                           hidden_seed)
-from ep_testutil import draw, u8, u16
+from ep_testutil import assert_bits_equal, draw, u8, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -84,52 +84,80 @@ def test_dispatch_fp8_small(w):
     assert np.array_equal(s.view(np.uint32), s_ref.view(np.uint32))
 
 
-@pytest.mark.parametrize("name", ["bf16", "zipf", "rt"])
-def test_dispatch_bf16_full_size_sampled(name):
+FULL = ["tiny", "bf16", "fp8", "zipf", "rt"]
+_SENTINEL_BF16 = -7.0  # rows past N_exp must keep it
+_SENTINEL_CODE = 0x5A
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_dispatch_bf16_full_size(name):
+    """The whole expanded layout (token rows and zeroed padding rows) of each
+    full-size workload, in the benchmark's launch configuration (worst-case
+    capacity, zero padding), bit for bit against the oracle; rows past N_exp
+    untouched."""
     w = WORKLOADS[name]
     idx, wts, x = draw(w)
     pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
     h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
-    cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)  # the benchmark's launch: worst-case capacity
-    recv, _ = ep.dispatch(h, bits_to_bf16_tensor(x).cuda(), "bf16", True, capacity=cap)
+    cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
+    buf = torch.full((cap, w.H), _SENTINEL_BF16, dtype=torch.bfloat16, device="cuda")
+    recv, _ = ep.dispatch(h, bits_to_bf16_tensor(x).cuda(), "bf16", True, recv_x=buf)
     assert h.sync_status() == ep.EP_OK
-    rng = np.random.default_rng(5)
-    rows = rng.choice(pl.num_expanded, size=3000, replace=False)
-    rows = np.concatenate([rows, np.nonzero(pl.exp_src < 0)[0][:500], [0, pl.num_expanded - 1]])
-    sub = oracle.Plan(**{**pl.__dict__, "exp_src": pl.exp_src[rows].copy(),
-                         "expert_offsets": np.array([0, len(rows)], np.int32)})
-    ref = oracle.dispatch_bf16(x, sub)
-    got = u16(recv[torch.from_numpy(rows).cuda()])
-    assert np.array_equal(got, ref)
-    # properties at any size: every real row equals its source row
-    src = torch.from_numpy(pl.exp_src).cuda().long()
-    real = src >= 0
-    xt = bits_to_bf16_tensor(x).cuda()
-    assert torch.equal(recv[: pl.num_expanded][real].view(torch.int16), xt[src[real]].view(torch.int16))
-    assert not recv[: pl.num_expanded][~real].view(torch.int16).any()
+    with oracle.parallel():
+        ref = oracle.dispatch_bf16(x, pl, True)
+    assert_bits_equal(recv[: pl.num_expanded], ref, f"{name} recv_x")
+    assert torch.all(recv[pl.num_expanded:] == _SENTINEL_BF16)
 
 
-def test_dispatch_fp8_full_size_sampled():
-    w = WORKLOADS["fp8"]
+@pytest.mark.parametrize("name", FULL)
+def test_dispatch_fp8_full_size(name):
+    """FP8 dispatch (quantised inside) of each full-size workload's hidden
+    states: every E4M3 code and every fp32 scale of the expanded layout bit
+    for bit against the oracle; rows past N_exp untouched."""
+    w = WORKLOADS[name]
+    assert w.H % 128 == 0
     idx, wts, x = draw(w)
     pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
     h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
     cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
-    recv, scales = ep.dispatch(h, bits_to_bf16_tensor(x).cuda(), "fp8", True, capacity=cap)
+    codes = torch.full((cap, w.H), _SENTINEL_CODE, dtype=torch.uint8, device="cuda")
+    scales = torch.full((cap, w.H // 128), -3.0, dtype=torch.float32, device="cuda")
+    recv, sc = ep.dispatch(h, bits_to_bf16_tensor(x).cuda(), "fp8", True,
+                           recv_x=codes.view(torch.float8_e4m3fn), recv_scales=scales)
     assert h.sync_status() == ep.EP_OK
-    rng = np.random.default_rng(6)
-    rows = np.concatenate([rng.choice(pl.num_expanded, size=3000, replace=False),
-                           np.nonzero(pl.exp_src < 0)[0][:300]])
-    sub = oracle.Plan(**{**pl.__dict__, "exp_src": pl.exp_src[rows].copy(),
-                         "expert_offsets": np.array([0, len(rows)], np.int32)})
-    q_ref, s_ref = oracle.dispatch_fp8(x, sub)
-    r = torch.from_numpy(rows).cuda()
-    assert np.array_equal(u8(recv[r]), q_ref)
-    assert np.array_equal(scales[r].cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+    with oracle.parallel():
+        q_ref, s_ref = oracle.dispatch_fp8(x, pl, True)
+    n = pl.num_expanded
+    assert_bits_equal(codes[:n], q_ref, f"{name} codes")
+    assert_bits_equal(scales[:n], s_ref, f"{name} scales")
+    assert torch.all(codes[n:] == _SENTINEL_CODE) and torch.all(scales[n:] == -3.0)
+
+
+def test_cached_dispatch_zipf_ten_steps_full_size():
+    """The skewed-routing workload at full size: a fresh plan and dispatch,
+    then 10 cached-handle dispatches with new hidden states (the seeds of
+    dispatches 1..10), each whole array against the oracle on the same plan."""
+    w = WORKLOADS["zipf"]
+    idx, wts = draw_topk(w)
+    pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
+    cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
+    x0 = draw_hidden(w.T, w.H, hidden_seed(w, 0))
+    h, recv, _ = ep.dispatch_fresh(torch.from_numpy(idx).cuda(), bits_to_bf16_tensor(x0).cuda(),
+                                   w.P, w.E, w.A)  # outputs sized for the worst case
+    assert recv.shape[0] == cap
+    assert h.sync_status() == ep.EP_OK
+    with oracle.parallel():
+        assert_bits_equal(recv[: pl.num_expanded], oracle.dispatch_bf16(x0, pl, True), "zipf fresh")
+    for step in range(1, w.cached_steps + 1):
+        x = draw_hidden(w.T, w.H, hidden_seed(w, step))
+        recv, _ = ep.dispatch_cached(h, bits_to_bf16_tensor(x).cuda(), w.E, w.A, w.S, recv_x=recv)
+        assert h.sync_status() == ep.EP_OK
+        with oracle.parallel():
+            assert_bits_equal(recv[: pl.num_expanded], oracle.dispatch_bf16(x, pl, True), f"zipf cached {step}")
 
 
 def test_cached_dispatch_zipf_ten_steps():
-    """Fresh plan, then 10 cached-handle dispatches with new x (seeds 1..10)."""
+    """Fresh plan, then 10 cached-handle dispatches with new x (seeds 1..10), at a reduced size."""
     w = WORKLOADS["zipf"].scaled(S=32, H=1024)
     idx, wts = draw_topk(w)
     pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
@@ -254,42 +282,28 @@ def test_combine_y_rows_capacity_error():
     assert h.sync_status() == ep.EP_ERR_CAPACITY
 
 
-@pytest.mark.parametrize("name,kind", [("bf16", "identity"), ("fp8", "dequant"), ("zipf", "identity"),
-                                       ("rt", "scale")])
-def test_round_trip_full_size_sampled(name, kind):
-    """Full-size workloads in the benchmark's launch configuration (worst-case
-    capacity, zero padding); the oracle computes a sample of tokens, each from
-    its own dispatch of only the rows those tokens need."""
+@pytest.mark.parametrize("name", FULL)
+def test_round_trip_full_size(name):
+    """Each full-size workload end to end in the benchmark's launch
+    configuration (worst-case capacity, zero padding): dispatch (FP8 for the
+    FP8 workload), the workload's synthetic expert, combine; the whole [T,H]
+    output against the oracle's own dispatch -> expert -> combine, within the
+    combine tolerance and in fact bit for bit."""
     w = WORKLOADS[name]
+    kind = w.expert
     idx, wts, x = draw(w)
     pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
     h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
     cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
-    recv, scales = ep.dispatch(h, bits_to_bf16_tensor(x).cuda(), "fp8" if kind == "dequant" else "bf16",
-                               True, capacity=cap)
+    recv, scales = ep.dispatch(h, bits_to_bf16_tensor(x).cuda(), "fp8" if w.fp8 else "bf16", True, capacity=cap)
     y = _gpu_expert(kind, recv, scales, h.field("expert_offsets"), w.E)
     out = ep.combine(h, y, torch.from_numpy(wts).cuda())
     assert h.sync_status() == ep.EP_OK
-    rng = np.random.default_rng(7)
-    toks = np.sort(rng.choice(w.T, size=600, replace=False))
-    rows = np.unique(pl.slot[toks][pl.slot[toks] >= 0])
-    # oracle y for just those rows: a one-segment plan over the needed rows
-    remap = -np.ones(pl.num_expanded, np.int64)
-    remap[rows] = np.arange(len(rows))
-    sub = oracle.Plan(**{**pl.__dict__, "exp_src": pl.exp_src[rows].copy(),
-                         "expert_offsets": np.array([0, len(rows)], np.int32)})
-    if kind == "scale":
-        e_of_row = (np.searchsorted(pl.expert_offsets, rows, side="right") - 1).astype(np.int32)
-        y_rows = oracle.expert_scale_rows(oracle.dispatch_bf16(x, sub), e_of_row, w.E)
-    else:
-        y_rows = _oracle_expert(kind, sub, x)
-    sl = pl.slot[toks]
-    sub_slot = np.where(sl >= 0, remap[np.maximum(sl, 0)], -1).astype(np.int32)
-    tp = oracle.Plan(**{**pl.__dict__, "slot": np.ascontiguousarray(sub_slot), "S": len(toks), "P": 1})
-    ref = oracle.combine(y_rows, tp, np.ascontiguousarray(wts[toks]))
-    got = u16(out[torch.from_numpy(toks).cuda()])
+    with oracle.parallel():
+        ref = oracle.combine(_oracle_expert(kind, pl, x), pl, wts)
+    got = u16(out)
     np.testing.assert_allclose(_f32(got), _f32(ref), rtol=RTOL, atol=ATOL)
-    assert np.array_equal(got, ref)
+    assert_bits_equal(out, ref, f"{name} combine")
 
 
 def _midpoint_stress_rows(T, H, seed):
@@ -339,3 +353,65 @@ def test_dispatch_fp8_rounding_midpoints_and_tiny_groups():
     q = u8(recv)
     bad = np.argwhere(q != q_ref)
     assert len(bad) == 0, f"{len(bad)} codes differ, first {bad[:3].tolist()}"
+
+
+def _non_finite_rows(T, H, seed):
+    """N(0,1) bf16 rows with non-finite elements planted group by group: one
+    NaN of either sign, +inf or -inf, a group of NaNs, zeros with a NaN, and
+    inf, -inf and NaN together."""
+    rng = np.random.default_rng(seed)
+    bits = draw_hidden(T, H, seed)
+    G = H // 128
+    kinds = rng.integers(0, 8, size=(T, G))
+    pos = rng.integers(0, 128, size=(T, G, 3))
+    PNAN, NNAN, PINF, NINF = 0x7FC0, 0xFFC0, 0x7F80, 0xFF80
+    for t in range(T):
+        for j in range(G):
+            g = bits[t, j * 128:(j + 1) * 128]
+            a, b, c = pos[t, j]
+            k = kinds[t, j]
+            if k == 1:
+                g[a] = PNAN
+            elif k == 2:
+                g[a] = NNAN
+            elif k == 3:
+                g[a] = PINF
+            elif k == 4:
+                g[a] = NINF
+            elif k == 5:
+                g[:] = PNAN
+            elif k == 6:
+                g[:] = 0
+                g[a] = NNAN
+            elif k == 7:
+                g[a], g[b], g[c] = PINF, NINF, NNAN
+    return bits
+
+
+@pytest.mark.parametrize("w", [WORKLOADS["tiny"].scaled(H=1024), WORKLOADS["fp8"].scaled(S=40, H=2048)],
+                         ids=["tiny", "fp8"])
+def test_non_finite_hidden_values(w):
+    """Inf and NaN in x, under the reading the oracle pins (NaN elements left
+    out of amax, an infinite element makes the scale +inf, every NaN quotient
+    is code 0x7F): FP8 codes and scales and the BF16 bit copy bit for bit
+    against the oracle; the combine equal wherever the oracle is not NaN, and
+    NaN exactly where the oracle is."""
+    idx, wts = draw_topk(w)
+    x = _non_finite_rows(w.T, w.H, seed=29)
+    pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
+    h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
+    xt = bits_to_bf16_tensor(x).cuda()
+    q, sc = ep.dispatch(h, xt, "fp8")
+    recv, _ = ep.dispatch(h, xt, "bf16")
+    out = ep.combine(h, recv, torch.from_numpy(wts).cuda())
+    assert h.sync_status() == ep.EP_OK
+    q_ref, s_ref = oracle.dispatch_fp8(x, pl)
+    assert_bits_equal(q.view(torch.uint8), q_ref, "codes")
+    assert_bits_equal(sc, s_ref, "scales")
+    assert (q_ref == 0x7F).any() and np.isinf(s_ref).any()
+    assert_bits_equal(recv, oracle.dispatch_bf16(x, pl), "bf16 rows")
+    ref = oracle.combine(oracle.dispatch_bf16(x, pl), pl, wts)
+    got = u16(out)
+    nan_ref, nan_got = np.isnan(_f32(ref)), np.isnan(_f32(got))
+    assert nan_ref.any() and np.array_equal(nan_got, nan_ref)
+    assert np.array_equal(got[~nan_ref], ref[~nan_ref])

@@ -152,6 +152,36 @@ def test_barrier_timeout_is_reported_and_recoverable():
     assert_plan_equal(gpu_plan_arrays(h), oracle.plan(idx, w.S, w.P, w.E, w.A))
 
 
+def test_replan_right_after_a_timeout_does_no_barrier_work():
+    """A plan whose grid-barrier wait ran out leaves its arrivals in the
+    barrier count.  Plans enqueued right after it, with no status read in
+    between, must not pass a barrier on those arrivals: they find the
+    timed-out mark and arrive at no barrier, the status stays EP_ERR_TIMEOUT,
+    and a dispatch on the unfinished plan writes nothing past its capacity.
+    Reading the status clears the control words; the next plan is correct."""
+    w = WORKLOADS["bf16"].scaled(S=200)  # 1600 tokens -> 7 tiles, a grid of more CTAs
+    idx, _ = draw_topk(w)
+    idx2, _ = draw_topk(w, seed=5)
+    t, t2 = torch.from_numpy(idx).cuda(), torch.from_numpy(idx2).cuda()
+    try:
+        ep.set_plan_wait_debug(poll_limit=2000, suppress_tile=2)
+        h = ep.plan(t, w.P, w.E, w.A)
+    finally:
+        ep.set_plan_wait_debug(0, -1)
+    h.replan(t2)  # no status read in between
+    h.replan(t2)
+    H = 256
+    cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
+    x = torch.randn((w.T, H), device="cuda").to(torch.bfloat16)
+    buf = torch.full((cap + 64, H), 5.0, dtype=torch.bfloat16, device="cuda")
+    ep.dispatch(h, x, "bf16", True, recv_x=buf[:cap])
+    assert h.sync_status() == ep.EP_ERR_TIMEOUT
+    assert torch.all(buf[cap:] == 5.0)
+    h.replan(t2)
+    assert h.sync_status() == ep.EP_OK
+    assert_plan_equal(gpu_plan_arrays(h), oracle.plan(idx2, w.S, w.P, w.E, w.A))
+
+
 def test_worst_expanded_rows_bounds_exact_size():
     for name in ["tiny", "bf16", "fp8", "zipf", "rt"]:
         w = WORKLOADS[name]

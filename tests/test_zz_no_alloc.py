@@ -8,8 +8,10 @@ passes every output buffer, and the plan's scratch lives in a fixed array
 inside the library.  This test calls it through the C ABI twice in a row
 (different routing each time, so stale scratch from the first call would
 show) and checks every plan array against the one ep_plan produces for the
-same routing.  It is collected last, runs alone in a fresh process as well
-as after the other tests, and allocates all its buffers before the call.
+same routing, and against the oracle directly (default and explicit channel
+counts, expert alignment 1).  It is collected last, runs alone in a fresh
+process as well as after the other tests, and allocates all its buffers
+before the call.
 """
 import ctypes
 
@@ -18,8 +20,9 @@ import pytest
 import torch
 
 import combine_ep_plan_gb300 as ep
+import oracle
 from combine_ep_plan_gb300.inputs import WORKLOADS, draw_topk
-from ep_testutil import PLAN_FIELDS, gpu_plan_arrays
+from ep_testutil import PLAN_FIELDS, assert_plan_equal, gpu_plan_arrays
 
 pytestmark = pytest.mark.gpu
 
@@ -97,6 +100,31 @@ def test_static_scratch_plan_matches_ep_plan_twice_in_a_row(lib, name):
         for k in PLAN_FIELDS + ["pad_rows"]:
             assert np.array_equal(got[k], want[k]), k
         h.destroy()
+
+
+@pytest.mark.parametrize("name,C,A", [("tiny", 0, 1), ("bf16", 5, 128), ("rt", 16, 1)])
+def test_static_scratch_plan_matches_the_oracle(lib, name, C, A):
+    """Every plan array of the allocation-free entry point against the oracle
+    directly: the default channel count, an explicit one other than 16, and
+    expert_alignment 1 (no padding rows: the one-entry pad_rows buffer)."""
+    w = WORKLOADS[name].scaled(A=A)
+    Cq = C if C else min(16, w.S)
+    idx, _ = draw_topk(w, seed=13)
+    idx_t = torch.from_numpy(idx).cuda()
+    bufs = _buffers(w, Cq)
+    st = PlanBuffers(**{k: v.data_ptr() for k, v in bufs.items()})
+    torch.cuda.synchronize()
+    rc = lib.ep_plan_static_scratch(idx_t.data_ptr(), w.S, w.P, w.K, w.E, w.A, C, ctypes.byref(st),
+                                    torch.cuda.current_stream().cuda_stream)
+    assert rc == ep.EP_OK
+    torch.cuda.synchronize()
+    n_recv, n_exp, n_pad, status = bufs["info"].tolist()
+    assert status == 0
+    got = {k: v.cpu().numpy() for k, v in bufs.items()}
+    got["recv_src_idx"] = got["recv_src_idx"][:n_recv]
+    got["exp_src"] = got["exp_src"][:n_exp]
+    got["pad_rows"] = got["pad_rows"][:n_pad]
+    assert_plan_equal(got, oracle.plan(idx, w.S, w.P, w.E, w.A, Cq))
 
 
 def test_static_scratch_rejects_plans_beyond_its_limit(lib):
