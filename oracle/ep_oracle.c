@@ -561,6 +561,7 @@ void ep_oracle_combine_backward(const uint16_t *grad_out, const uint16_t *y, int
             if (exp_src[r] < 0)
                 for (int64_t h = 0; h < H; ++h)
                     grad_y[r * H + h] = 0;
+#pragma omp parallel for schedule(static)
     for (int64_t g = 0; g < T; ++g)
         for (int k = 0; k < K; ++k) {
             int32_t r = slot[g * K + k];

@@ -55,6 +55,7 @@ def test_parallel_build_is_bit_identical(name):
         "expert_scale": lambda: oracle.expert_scale(y, pl),
         "expert_dequant": lambda: oracle.expert_dequant(*oracle.dispatch_fp8(x, pl, True)),
         "dispatch_backward": lambda: oracle.dispatch_backward(y, pl),
+        "combine_backward": lambda: oracle.combine_backward(bias, y, pl, wts, True),
     }
     q, s = oracle.dispatch_fp8(x, pl, True)
     cases["dispatch_fp8_input"] = lambda: oracle.dispatch_fp8_input(q[: pl.T], s[: pl.T], pl, True)
