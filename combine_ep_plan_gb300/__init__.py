@@ -617,7 +617,8 @@ def summarize_profile(records) -> list:
     CTA start to the last CTA end (ns), median and max CTA duration (ns),
     payload GB/s over the span, and for the plan the median stage offsets
     from the launch's first start, in ns: route scan over the CTAs that
-    scanned a tile, each grid barrier passed over all CTAs."""
+    scanned a tile, each grid barrier passed over all CTAs (a one-CTA plan:
+    route scan, column counts, offsets)."""
     import numpy as np
     r = np.asarray(records.cpu() if isinstance(records, torch.Tensor) else records).astype(np.uint64)
     if r.size == 0:
@@ -638,11 +639,15 @@ def summarize_profile(records) -> list:
                "gbs": nbytes / span if span > 0 else 0.0}
         if k == 1:
             # route scan over the CTAs that scanned a tile (the others have
-            # no scan mark); the two grid barriers over all CTAs
+            # no scan mark); the two grid barriers over all CTAs.  A one-tile
+            # plan runs as one CTA without grid barriers: its marks are the
+            # column counts and the offsets instead.
             base = t0.min()
             tiles = r[m, 2] > 0
-            for name, col, sel in (("scan_ns", 2, tiles), ("barrier1_ns", 3, np.ones_like(tiles)),
-                                   ("barrier2_ns", 4, np.ones_like(tiles))):
+            one = int(m.sum()) == 1
+            for name, col, sel in (("scan_ns", 2, tiles),
+                                   ("counts_ns" if one else "barrier1_ns", 3, np.ones_like(tiles)),
+                                   ("offsets_ns" if one else "barrier2_ns", 4, np.ones_like(tiles))):
                 v = r[m, col].astype(np.int64)[sel]
                 v = v[v > 0]
                 row[name] = float(np.median(v - base)) if len(v) else 0.0

@@ -191,12 +191,25 @@ __device__ __forceinline__ int x_at(const PlanDev& p, int col, int64_t g) {
          __popc(__ldcg(&p.tile_bits[at]) & lanes_below(gl & 31));
 }
 
-// One warp turns the column totals into the offsets, in shared memory:
-// expert segments padded to A (exp_off), padding rows per expert (pad_off)
-// and receive windows (recv_off), each an exclusive scan with its total at
-// the end; sizes[] gets {N_recv, N_exp, N_pad}.  Each lane scans a
-// contiguous run of each array, one shuffle scan joins the lanes.
-__device__ void offsets_warp_scan(const PlanDev& p, int* exp_off, int* pad_off, int* recv_off, int* sizes) {
+// Column total col, from global memory (written by other CTAs) or from the
+// CTA's own shared memory.
+template <bool SMEM>
+__device__ __forceinline__ int load_total(const int* tot, int col) {
+  if (SMEM) return tot[col];
+  return __ldcg(&tot[col]);
+}
+
+// One warp turns the column totals tot[P+E] (ranks, then experts) into the
+// offsets, in shared memory: expert segments padded to A (exp_off), padding
+// rows per expert (pad_off) and receive windows (recv_off), each an
+// exclusive scan with its total at the end; sizes[] gets {N_recv, N_exp,
+// N_pad}.  Each lane scans a contiguous run of each array, one shuffle scan
+// joins the lanes.  The first batch of rank totals is loaded together with
+// the first batch of expert totals (one round trip up to 256 experts and
+// 256 ranks).
+template <bool SMEM>
+__device__ void offsets_warp_scan(const PlanDev& p, const int* tot, int* exp_off, int* pad_off, int* recv_off,
+                                  int* sizes) {
   const int lane = threadIdx.x & 31;
   const int per_e = (p.E + 31) / 32;
   const int per_d = (p.P + 31) / 32;
@@ -204,12 +217,18 @@ __device__ void offsets_warp_scan(const PlanDev& p, int* exp_off, int* pad_off, 
   const int lo_d = lane * per_d;
   int sum_exp = 0, sum_pad = 0, sum_recv = 0;
   constexpr int kBatch = 8;  // loads issued before any is used
+  int nd[kBatch];
+#pragma unroll
+  for (int u = 0; u < kBatch; ++u) {
+    const int d = lo_d + u;
+    nd[u] = (u < per_d && d < p.P) ? load_total<SMEM>(tot, d) : 0;
+  }
   for (int i0 = 0; i0 < per_e; i0 += kBatch) {
     int n[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int e = lo_e + i0 + u;
-      n[u] = (i0 + u < per_e && e < p.E) ? __ldcg(&p.totals[p.P + e]) : 0;
+      n[u] = (i0 + u < per_e && e < p.E) ? load_total<SMEM>(tot, p.P + e) : 0;
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
@@ -228,7 +247,7 @@ __device__ void offsets_warp_scan(const PlanDev& p, int* exp_off, int* pad_off, 
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int d = lo_d + i0 + u;
-      n[u] = (i0 + u < per_d && d < p.P) ? __ldcg(&p.totals[d]) : 0;
+      n[u] = i0 == 0 ? nd[u] : ((i0 + u < per_d && d < p.P) ? load_total<SMEM>(tot, d) : 0);
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
@@ -352,7 +371,7 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
   const bool own_tile = gridDim.x >= static_cast<unsigned>(p.num_tiles);
   const bool has_tile = own_tile && blockIdx.x < static_cast<unsigned>(p.num_tiles);
   if (threadIdx.x < 32) {
-    offsets_warp_scan(p, exp_off, pad_off, recv_off, s_sizes);
+    offsets_warp_scan<false>(p, p.totals, exp_off, pad_off, recv_off, s_sizes);
   } else if (has_tile) {
     // the own tile's exclusive prefix per column
     for (int col = threadIdx.x - 32; col < p.ncols; col += blockDim.x - 32)
@@ -558,6 +577,159 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
   if (PROF) prof_cta_end(p, kProfPlan, t_start, t_scan, t_bar1, t_bar2, scanned, 0);
 }
 
+// X_col(g) of a one-tile plan, all in shared memory: the word prefix of g's
+// word plus the bits before g in it; g == T gives the column total.
+__device__ __forceinline__ int x_one(const uint32_t* bits, const int* wpre, const int* tot, int ncols, int col,
+                                     int g, int T) {
+  if (g >= T) return tot[col];
+  const int at = (g >> 5) * ncols + col;
+  return wpre[at] + __popc(bits[at] & lanes_below(g & 31));
+}
+
+// The whole plan of at most one tile (T <= 256 tokens) in one CTA, with every
+// intermediate in shared memory: the bit matrix, each word's prefix inside
+// the column, the column totals and the offsets.  The only global loads are
+// the routing ids; every output is a store.  (The general kernel with one
+// CTA computes the same through global scratch: a chain of L2 round trips.)
+// PROF marks: [2] route scan done, [3] column counts done, [4] offsets done.
+template <bool PROF, int KMAX>
+__global__ void __launch_bounds__(kTile, 1) ep_plan_one_tile_kernel(PlanDev p) {
+  extern __shared__ __align__(16) uint32_t smem[];
+  unsigned long long t_start = 0, t_scan = 0, t_count = 0, t_off = 0;
+  if (PROF && threadIdx.x == 0) t_start = prof_now();
+  const int nc = p.ncols;
+  const int T = static_cast<int>(p.T);
+  uint32_t* bits = smem;                                      // [kTileWords][ncols]
+  int* wpre = reinterpret_cast<int*>(bits + kTileWords * nc);  // [kTileWords][ncols]
+  int* tot = wpre + kTileWords * nc;                           // [ncols]
+  int* ids = tot + nc;                                         // [kTile * K], then the slots
+  int* exp_off = ids + kTile * p.K;                            // [E+1]
+  int* pad_off = exp_off + (p.E + 1);                          // [E+1]
+  int* recv_off = pad_off + (p.E + 1);                         // [P+1]
+  __shared__ int s_sizes[3];
+
+  for (int i = threadIdx.x; i < kTileWords * nc; i += blockDim.x) bits[i] = 0u;
+  load_tile_ids<KMAX>(p, 0, ids);
+  __syncthreads();
+  build_tile_bits(p, ids, bits);
+  __syncthreads();
+  if (PROF && threadIdx.x == 0) t_scan = prof_now();
+  for (int col = threadIdx.x; col < nc; col += blockDim.x) {
+    int n = 0;
+#pragma unroll
+    for (int j = 0; j < kTileWords; ++j) {
+      wpre[j * nc + col] = n;
+      n += __popc(bits[j * nc + col]);
+    }
+    tot[col] = n;
+    p.totals[col] = n;
+  }
+  __syncthreads();
+  if (PROF && threadIdx.x == 0) t_count = prof_now();
+  if (threadIdx.x < 32) {
+    offsets_warp_scan<true>(p, tot, exp_off, pad_off, recv_off, s_sizes);
+  } else {
+    // the outputs that need no offsets, while warp 0 scans: the prefix
+    // matrices and per-source expert counts
+    const int tid = threadIdx.x - 32, nthr = blockDim.x - 32;
+    const int S = static_cast<int>(p.S);
+    for (int i = tid; i < p.P * p.P * p.C; i += nthr) {
+      const int c = i % p.C;
+      const int sd = i / p.C;
+      const int d = sd % p.P;
+      const int s = sd / p.P;
+      const int src0 = s * S;
+      const int lo = src0 + static_cast<int>(min64(p.S, static_cast<int64_t>(c) * p.chunk));
+      const int hi = src0 + static_cast<int>(min64(p.S, static_cast<int64_t>(c + 1) * p.chunk));
+      const int x0 = x_one(bits, wpre, tot, nc, d, src0, T);
+      p.rcpm[(d * p.P + s) * p.C + c] = x_one(bits, wpre, tot, nc, d, lo, T);
+      p.cpm[i] = x_one(bits, wpre, tot, nc, d, hi, T) - x0;
+      if (c == 0) {
+        const int x1 = x_one(bits, wpre, tot, nc, d, src0 + S, T);
+        p.rpm[s * p.P + d] = x1;
+        p.ntpr[s * p.P + d] = x1 - x0;
+      }
+    }
+    for (int i = tid; i < p.P * p.E; i += nthr) {
+      const int s = i / p.E;
+      const int e = i - s * p.E;
+      p.ntpe[i] = x_one(bits, wpre, tot, nc, p.P + e, (s + 1) * S, T) - x_one(bits, wpre, tot, nc, p.P + e, s * S, T);
+    }
+  }
+  __syncthreads();
+  if (PROF && threadIdx.x == 0) t_off = prof_now();
+  const int n_pad = s_sizes[kSizePad];
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+    p.exp_off[i] = exp_off[i];
+    p.pad_off[i] = pad_off[i];
+  }
+  for (int i = threadIdx.x; i <= p.P; i += blockDim.x) p.recv_off[i] = recv_off[i];
+  if (threadIdx.x == 0) {
+    p.sizes[kSizeRecv] = s_sizes[kSizeRecv];
+    p.sizes[kSizeExp] = s_sizes[kSizeExp];
+    p.sizes[kSizePad] = n_pad;
+  }
+  // slots and exp_src, one token per thread; each slot replaces its id in
+  // shared memory and the block leaves as one contiguous store
+  if (threadIdx.x < T) {
+    const int i = threadIdx.x;
+    for (int k = 0; k < p.K; ++k) {
+      const int e = ids[i * p.K + k];
+      int r = -1;
+      if (e >= 0) {
+        r = exp_off[e] + x_one(bits, wpre, tot, nc, p.P + e, i, T);
+        if (in_cap(r, p.cap_exp)) {
+          p.exp_src[r] = i;
+        } else {
+          atomicOr(&p.ctr[kCtrStatus], kStCapacity);
+          r = -1;
+        }
+      }
+      ids[i * p.K + k] = r;
+    }
+  }
+  // dense [T,P]: is_token_in_rank, send_head, recv_src_idx; consecutive
+  // threads take consecutive ranks of a token (coalesced rows)
+  for (int i = threadIdx.x; i < T * p.P; i += blockDim.x) {
+    const int g = i / p.P;
+    const int d = i - g * p.P;
+    const int at = (g >> 5) * nc + d;
+    const int bit = (bits[at] >> (g & 31)) & 1;
+    const int pos = wpre[at] + __popc(bits[at] & lanes_below(g & 31));
+    p.in_rank[i] = static_cast<unsigned char>(bit);
+    p.send_head[i] = bit ? pos : -1;
+    if (bit) {
+      const int64_t at_r = static_cast<int64_t>(recv_off[d]) + pos;
+      if (in_cap(at_r, p.cap_recv))
+        p.recv_src_idx[at_r] = static_cast<int>(g % p.S);
+      else
+        atomicOr(&p.ctr[kCtrStatus], kStCapacity);
+    }
+  }
+  // padding rows of the expanded layout
+  const int n_pad_w = n_pad < p.cap_pad ? n_pad : static_cast<int>(p.cap_pad);
+  if (threadIdx.x == 0 && n_pad > p.cap_pad) atomicOr(&p.ctr[kCtrStatus], kStCapacity);
+  for (int i = threadIdx.x; i < n_pad_w; i += blockDim.x) {
+    int lo = 0, hi = p.E;  // e with pad_off[e] <= i < pad_off[e+1]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (pad_off[mid] <= i) lo = mid; else hi = mid;
+    }
+    const int n_e = (exp_off[lo + 1] - exp_off[lo]) - (pad_off[lo + 1] - pad_off[lo]);
+    const int row = exp_off[lo] + n_e + (i - pad_off[lo]);
+    p.pad_rows[i] = row;
+    if (in_cap(row, p.cap_exp))
+      p.exp_src[row] = -1;
+    else
+      atomicOr(&p.ctr[kCtrStatus], kStCapacity);
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < T * p.K; j += blockDim.x) p.slot[j] = ids[j];
+  if (PROF)  // units: the tokens scanned, counted once (prof_cta_end sums over the warps)
+    prof_cta_end(p, kProfPlan, t_start, t_scan, t_count, t_off,
+                 threadIdx.x == 0 ? static_cast<unsigned long long>(T) : 0ull, 0);
+}
+
 }  // namespace
 
 size_t plan_smem_bytes(int P, int E, int K) {
@@ -565,6 +737,13 @@ size_t plan_smem_bytes(int P, int E, int K) {
   // phase 2: the offsets and the own tile's slots
   return sizeof(uint32_t) * kTileWords * (P + E) + sizeof(int) * (kTile * K + (P + E)) +
          sizeof(int) * (2 * (E + 1) + (P + 1) + kTile * K);
+}
+
+// Shared memory of the one-tile kernel: bit matrix, word prefixes, totals,
+// ids (then slots) and the offsets.
+size_t plan_one_tile_smem_bytes(int P, int E, int K) {
+  return sizeof(uint32_t) * kTileWords * (P + E) * 2 + sizeof(int) * (P + E) + sizeof(int) * kTile * K +
+         sizeof(int) * (2 * (E + 1) + (P + 1));
 }
 
 // Phase-2 outputs per CTA that size the grid (tuning knob).
@@ -607,8 +786,30 @@ int plan_grid(const PlanDev& p, int sm_budget) {
   return static_cast<int>(grid);
 }
 
+// The largest dynamic shared memory a CTA may ask for on this device.
+size_t max_dyn_smem() {
+  int dev = 0, v = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return 48 * 1024;
+  return static_cast<size_t>(v);
+}
+
 template <bool PROF, int KMAX>
 cudaError_t launch_plan_t(const PlanDev& p, cudaStream_t stream, const LaunchCfg& cfg) {
+  if (p.num_tiles == 1) {
+    const size_t smem1 = plan_one_tile_smem_bytes(p.P, p.E, p.K);
+    if (smem1 <= max_dyn_smem()) {
+      if (smem1 > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(ep_plan_one_tile_kernel<PROF, KMAX>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem1));
+        if (err != cudaSuccess) return err;
+      }
+      if (cfg.ctas) *cfg.ctas = 1;
+      ep_plan_one_tile_kernel<PROF, KMAX><<<1, kTile, smem1, stream>>>(p);
+      return cudaGetLastError();
+    }
+  }
   const size_t smem = plan_smem_bytes(p.P, p.E, p.K);
   if (smem > 48 * 1024) {
     cudaError_t err = cudaFuncSetAttribute(ep_plan_kernel<PROF, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -486,7 +486,9 @@ ep_status_t ep_pending_wait(ep_pending_t pending, int64_t *num_expanded_host,
  *       pre-quantised FP8, 5 combine, 6 dispatch backward
  *   [1] start, [5] end: device global timer, ns
  *   [2] [3] [4] stage marks (plan: route scan of the CTA's last tile done,
- *       first grid barrier passed, second grid barrier passed; 0 for the
+ *       first grid barrier passed, second grid barrier passed; a plan of at
+ *       most 256 tokens runs as one CTA without grid barriers and marks the
+ *       route scan, the column counts and the offsets instead; 0 for the
  *       other kernels)
  *   [6] work units: plan, tokens scanned; others, (row, column chunk) items
  *   [7] payload bytes read and written by the CTA (hidden rows, codes, scales,
