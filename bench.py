@@ -247,57 +247,72 @@ def oracle_pass(w, idx, wts, x):
     return pl
 
 
-def oracle_sample(w, min_seconds: float):
-    """Whole-workload oracle passes until min_seconds of CPU work -> GB/s."""
+def oracle_sample(w, min_seconds: float, parallel: bool = False):
+    """Whole-workload oracle passes until min_seconds of CPU work -> GB/s.
+    parallel: the OpenMP build of the same source (all host threads)."""
+    import oracle
     from combine_ep_plan_gb300.inputs import draw_hidden, draw_topk, hidden_seed
     idx, wts = draw_topk(w)
     x = draw_hidden(w.T, w.H, hidden_seed(w))
     times = []
     pl = None
-    t_start = time.perf_counter()
-    while not times or time.perf_counter() - t_start < min_seconds:
-        t0 = time.perf_counter()
-        pl = oracle_pass(w, idx, wts, x)
-        times.append(time.perf_counter() - t0)
+    with oracle.parallel(parallel):
+        threads = oracle.threads()
+        t_start = time.perf_counter()
+        while not times or time.perf_counter() - t_start < min_seconds:
+            t0 = time.perf_counter()
+            pl = oracle_pass(w, idx, wts, x)
+            times.append(time.perf_counter() - t0)
     n_valid = int(np.sum(pl.slot >= 0))
     led = step_ledger(w, pl.num_expanded, n_valid, pl.num_recv_total)
     t = statistics.mean(times)
-    return {"gbs": led["total"] / t / 1e9, "tokens_per_s": w.T / t, "seconds_per_pass": t, "passes": len(times)}
+    return {"gbs": led["total"] / t / 1e9, "tokens_per_s": w.T / t, "seconds_per_pass": t, "passes": len(times),
+            "threads": threads}
 
 
 def run_reference(args):
-    """The reference arm: the CPU oracle, as it stands, on the host cores."""
+    """The reference arm: the CPU oracle, as it stands, on the host cores
+    (its OpenMP build, every host thread)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    import oracle
     from combine_ep_plan_gb300.inputs import WORKLOADS, draw_hidden, draw_topk, hidden_seed
     full = WORKLOADS[args.workload]
+    parallel = oracle.omp_available()
+    with oracle.parallel(parallel):
+        threads = oracle.threads()
     # each step is a bounded sample of the workload: fewer tokens per rank, so
-    # that warmup + steps take about two minutes of single-threaded CPU time
-    est_full_s = 4.0 * full.T / 16384 * full.H / 7168 * full.K / 6 * (1 + 0.2 * full.cached_steps)
+    # that warmup + steps take about two minutes of CPU time (a full bf16 pass
+    # takes about 4 s on one core; the split loops scale with the threads)
+    per_thread = 4.0 / min(threads, 8) if parallel else 4.0
+    est_full_s = per_thread * full.T / 16384 * full.H / 7168 * full.K / 6 * (1 + 0.2 * full.cached_steps)
     budget = 120.0 / max(1, args.steps + args.warmup)
     S = int(max(8, min(full.S, full.S * budget / est_full_s)))
     w = full.scaled(S=S)
     idx, wts = draw_topk(w)
     x = draw_hidden(w.T, w.H, hidden_seed(w))
-    for _ in range(args.warmup):
-        oracle_pass(w, idx, wts, x)
-    t0 = time.perf_counter()
-    pl = None
-    for _ in range(args.steps):
-        pl = oracle_pass(w, idx, wts, x)
-    dt = time.perf_counter() - t0
+    with oracle.parallel(parallel):
+        for _ in range(args.warmup):
+            oracle_pass(w, idx, wts, x)
+        t0 = time.perf_counter()
+        pl = None
+        for _ in range(args.steps):
+            pl = oracle_pass(w, idx, wts, x)
+        dt = time.perf_counter() - t0
     n_valid = int(np.sum(pl.slot >= 0))
     led = step_ledger(w, pl.num_expanded, n_valid, pl.num_recv_total)
     gbs = led["total"] * args.steps / dt / 1e9
-    sample = f"{args.workload} workload with S={S} tokens/rank (T={w.T}) per step, single-threaded C oracle"
+    build = f"OpenMP C oracle, {threads} threads" if parallel else "single-threaded C oracle"
+    sample = f"{args.workload} workload with S={S} tokens/rank (T={w.T}) per step, {build}"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "tokens_per_s": w.T * args.steps / dt,
         "config": workload_config(full, sample_S=S),
-        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -329,101 +344,230 @@ def workload_config(w, sample_S=None) -> dict:
 # our arm
 # ---------------------------------------------------------------------------
 
+class Bench:
+    """One workload on the device: inputs resident in HBM, one handle
+    re-planned from topk_idx every step (ep_replan recomputes every plan array
+    without allocating), outputs sized for the worst case (no host sync), and
+    the expert outputs the combine reads, prepared once outside any timing."""
+
+    def __init__(self, ep, w, dev, stream):
+        import torch
+        from combine_ep_plan_gb300.inputs import bits_to_bf16_tensor, draw_hidden, draw_topk, hidden_seed
+        self.ep, self.w, self.dev, self.stream = ep, w, dev, stream
+        self.idx_np, self.w_np = draw_topk(w)
+        self.x_nps = [draw_hidden(w.T, w.H, hidden_seed(w, i)) for i in range(1 + w.cached_steps)]
+        self.idx_t = torch.from_numpy(self.idx_np).to(dev)
+        self.wts_t = torch.from_numpy(self.w_np).to(dev)
+        self.x_ts = [bits_to_bf16_tensor(xn).to(dev) for xn in self.x_nps]
+        self.out_dtype = "fp8" if w.fp8 else "bf16"
+        self.cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
+        self.recv = torch.empty((self.cap, w.H), dtype=torch.float8_e4m3fn if w.fp8 else torch.bfloat16, device=dev)
+        self.recv_sc = torch.empty((self.cap, w.H // 128), dtype=torch.float32, device=dev) if w.fp8 else None
+        self.out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
+        self.h = ep.plan(self.idx_t, w.P, w.E, w.A, stream=stream)
+        ep.dispatch(self.h, self.x_ts[0], self.out_dtype, True, recv_x=self.recv, recv_scales=self.recv_sc,
+                    stream=stream)
+        self.n_exp, self.n_recv = self.h.sizes(stream)
+        self.h.check(stream)
+        self.n_valid = int((self.idx_t >= 0).sum().item())
+        self.led = step_ledger(w, self.n_exp, self.n_valid, self.n_recv)
+        if w.expert == "identity":
+            self.y = self.recv
+        elif w.expert == "dequant":
+            self.y = (self.recv.float() * self.recv_sc.repeat_interleave(128, dim=1)).to(torch.bfloat16)
+        else:
+            e_of_row = torch.repeat_interleave(torch.arange(w.E, device=dev),
+                                               torch.diff(self.h.field("expert_offsets").long()))
+            self.y = torch.zeros((self.cap, w.H), dtype=torch.bfloat16, device=dev)
+            self.y[: len(e_of_row)] = (self.recv[: len(e_of_row)].float()
+                                       * (1.0 + e_of_row.float() / w.E)[:, None]).to(torch.bfloat16)
+        torch.cuda.synchronize()
+
+    def step(self, ev=None, hh=None, xs=None, idx=None, wts=None, o=None, st=None):
+        """Plan -> the fresh dispatch -> the cached dispatches -> combine.  ev:
+        five events, recorded at the start, after the plan, after the fresh
+        dispatch, after the last dispatch and after the combine."""
+        ep = self.ep
+        st = st or self.stream
+        hh = hh or self.h
+        xs = xs if xs is not None else self.x_ts
+        if ev is not None:
+            ev[0].record(st)
+        hh.replan(self.idx_t if idx is None else idx, stream=st)
+        if ev is not None:
+            ev[1].record(st)
+        for i, xi in enumerate(xs):
+            ep.dispatch(hh, xi, self.out_dtype, True, recv_x=self.recv, recv_scales=self.recv_sc, stream=st)
+            if ev is not None and i == 0:
+                ev[2].record(st)
+        if ev is not None:
+            ev[3].record(st)
+        ep.combine(hh, self.y, self.wts_t if wts is None else wts, out=self.out if o is None else o, stream=st)
+        if ev is not None:
+            ev[4].record(st)
+
+    def capture(self):
+        """One step captured in a CUDA graph (the library's launches of
+        replan, dispatch and combine), replayed on the bench stream."""
+        import torch
+        side = torch.cuda.Stream()
+        side.wait_stream(self.stream)
+        with torch.cuda.stream(side):
+            self.step(st=side)
+        self.stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step(st=torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        return g
+
+    def timed(self, steps: int, warmup: int, sampler=None, every: int = 4, graph: bool = False) -> dict:
+        """warmup untimed steps, then `steps` timed ones between two events.
+        Per-phase times come from events recorded between the kernels of every
+        `every`-th timed step: an event between two kernels serialises them (the
+        next launch can no longer overlap the end of the previous grid), so the
+        other steps carry none.  graph: the timed steps replay one captured step
+        (no host launch cost between kernels); the per-phase events then come
+        from a separate pass of directly launched steps."""
+        import torch
+        st = self.stream
+        if graph:
+            return self._timed_graph(steps, warmup, sampler, every)
+        for _ in range(warmup):
+            self.step()
+        torch.cuda.synchronize()
+        barrier()
+        events = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] if i % every == 0 else None
+                  for i in range(steps)]
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        t_wall0 = time.time()
+        start.record(st)
+        for i in range(steps):
+            self.step(events[i])
+        end.record(st)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        barrier()
+        if sampler is not None:
+            sampler.mark(t_wall0, t_wall1)
+        sampled = [e for e in events if e is not None]
+        return {"local_ms": start.elapsed_time(end), "phases": self._phases(sampled), "sampled": len(sampled),
+                "launch": "direct"}
+
+    def _phases(self, sampled) -> dict:
+        n_cached = self.w.cached_steps
+        ph = {
+            "plan": [e[0].elapsed_time(e[1]) for e in sampled],
+            "dispatch": [e[1].elapsed_time(e[2]) for e in sampled],
+            "combine": [e[3].elapsed_time(e[4]) for e in sampled],
+            "step": [e[0].elapsed_time(e[4]) for e in sampled],
+        }
+        if n_cached:
+            ph["cached_dispatch"] = [e[2].elapsed_time(e[3]) / n_cached for e in sampled]
+        return ph
+
+    def _timed_graph(self, steps, warmup, sampler, every) -> dict:
+        import torch
+        st = self.stream
+        g = self.capture()
+        for _ in range(warmup):
+            g.replay()
+        torch.cuda.synchronize()
+        barrier()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t_wall0 = time.time()
+        start.record(st)
+        for _ in range(steps):
+            g.replay()
+        end.record(st)
+        torch.cuda.synchronize()
+        t_wall1 = time.time()
+        barrier()
+        if sampler is not None:
+            sampler.mark(t_wall0, t_wall1)
+        local_ms = start.elapsed_time(end)
+        sampled = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(max(3, steps // every))]
+        for e in sampled:
+            self.step(e)
+        torch.cuda.synchronize()
+        del g
+        return {"local_ms": local_ms, "phases": self._phases(sampled), "sampled": len(sampled), "launch": "graph"}
+
+    def roofline(self, phases: dict) -> dict:
+        """The dominant kernel's algorithmic bytes per launch over its median
+        event time, against the measured copy bandwidth."""
+        w, led = self.w, self.led
+        peak, peak_src = hbm_peak()
+        disp_ms = statistics.median(phases["cached_dispatch"] if w.cached_steps else phases["dispatch"])
+        comb_ms = statistics.median(phases["combine"])
+        if disp_ms >= comb_ms:
+            kname = "ep_dispatch_fp8_kernel" if w.fp8 else "ep_dispatch_copy_kernel"
+            kfile, kbytes, kms = "ep_dispatch_kernels.cu", led["dispatch"], disp_ms
+        else:
+            kname, kfile, kbytes, kms = "ep_combine_kernel", "ep_combine_kernels.cu", led["combine"], comb_ms
+        achieved = kbytes / (kms / 1e3) / 1e9
+        return {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": profiled_traffic(kname, kfile, w.name), "algorithmic_bytes": kbytes}
+
+    def close(self):
+        import torch
+        self.h.destroy(self.stream)
+        torch.cuda.synchronize()
+
+
+def phase_stats(ph: dict) -> dict:
+    """Median and max (ms) of each phase over the sampled steps."""
+    out = {}
+    for k, v in ph.items():
+        out[k] = round(statistics.median(v), 5)
+        out[k + "_max"] = round(max(v), 5)
+    return out
+
+
+def workload_line(b: Bench, r: dict, world: int, steps: int) -> dict:
+    """A workload's numbers for the `workloads` object of the JSON line."""
+    w = b.w
+    peak, _ = hbm_peak()
+    agg = aggregate(b.led["total"], w.T, r["local_ms"], world, steps)
+    return {
+        "config": workload_config(w)["workload"], "steps": steps, "sampled_steps": r["sampled"],
+        "launch": "one captured step replayed from a CUDA graph" if r["launch"] == "graph"
+        else "direct launches from the host",
+        "ms_per_step": round(agg["ms_per_step"], 5), "gbs": round(agg["gbs"], 2),
+        "tokens_per_s": round(agg["tokens_per_s"], 1), "hbm_roofline_frac": round(agg["gbs"] / world / peak, 4),
+        "phases_ms": phase_stats(r["phases"]), "ledger_bytes_per_step": b.led,
+        "roofline": b.roofline(r["phases"]),
+    }
+
+
 def run_ours(args):
     import torch
 
     import combine_ep_plan_gb300 as ep
     from combine_ep_plan_gb300 import build as ep_build
-    from combine_ep_plan_gb300.inputs import WORKLOADS, bits_to_bf16_tensor, draw_hidden, draw_topk, hidden_seed
+    from combine_ep_plan_gb300.inputs import WORKLOADS, bits_to_bf16_tensor
 
     rank, world, local = dist_init(use_cuda=True)
     torch.cuda.set_device(local)
     ep_build.build()
     ep.load_library()
-    w = WORKLOADS[args.workload]
-    idx_np, w_np = draw_topk(w)
-    x_nps = [draw_hidden(w.T, w.H, hidden_seed(w, i)) for i in range(1 + w.cached_steps)]
-
+    if args.kernels:
+        return run_kernel_table(ep, args, local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-    idx_t = torch.from_numpy(idx_np).to(dev)
-    wts_t = torch.from_numpy(w_np).to(dev)
-    x_ts = [bits_to_bf16_tensor(xn).to(dev) for xn in x_nps]
-    x_t = x_ts[0]
-    out_dtype = "fp8" if w.fp8 else "bf16"
-    cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
-    recv = torch.empty((cap, w.H), dtype=torch.float8_e4m3fn if w.fp8 else torch.bfloat16, device=dev)
-    recv_sc = torch.empty((cap, w.H // 128), dtype=torch.float32, device=dev) if w.fp8 else None
-    out = torch.empty((w.T, w.H), dtype=torch.bfloat16, device=dev)
-
-    # one handle, re-planned from topk_idx every step (a fresh plan without
-    # allocation: ep_replan recomputes every plan array)
-    h = ep.plan(idx_t, w.P, w.E, w.A, stream=stream)
-    ep.dispatch(h, x_t, out_dtype, True, recv_x=recv, recv_scales=recv_sc, stream=stream)
-    n_exp, n_recv = h.sizes(stream)
-    h.check(stream)
-    n_valid = int((idx_t >= 0).sum().item())
-    led = step_ledger(w, n_exp, n_valid, n_recv)
-
-    # the expert outputs the combine reads: the dispatched rows themselves
-    # (identity), or rows prepared once here, outside any timed region
-    if w.expert == "identity":
-        y = recv
-    elif w.expert == "dequant":
-        y = (recv.float() * recv_sc.repeat_interleave(128, dim=1)).to(torch.bfloat16)
-    else:
-        e_of_row = torch.repeat_interleave(torch.arange(w.E, device=dev),
-                                           torch.diff(h.field("expert_offsets").long()))
-        y = torch.zeros((cap, w.H), dtype=torch.bfloat16, device=dev)
-        y[: len(e_of_row)] = (recv[: len(e_of_row)].float() * (1.0 + e_of_row.float() / w.E)[:, None]).to(
-            torch.bfloat16)
-
-    def step(ev=None, hh=h, xs=None, idx=idx_t, wts=wts_t, o=out):
-        xs = xs if xs is not None else x_ts
-        if ev is not None:
-            ev[0].record(stream)
-        hh.replan(idx, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        for xi in xs:  # the fresh dispatch, then the cached-handle dispatches with new x
-            ep.dispatch(hh, xi, out_dtype, True, recv_x=recv, recv_scales=recv_sc, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
-        ep.combine(hh, y, wts, out=o, stream=stream)
-        if ev is not None:
-            ev[3].record(stream)
-
     sampler = ClockSampler(local)
     sampler.start()
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    barrier()
 
-    # Per-phase kernel times come from events recorded between the kernels of
-    # every 4th timed step.  An event between two kernels serialises them (the
-    # next launch can no longer overlap the end of the previous grid), so the
-    # other steps carry none.
-    every = 4
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] if i % every == 0 else None
-              for i in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    t_wall0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        step(events[i])
-    end.record(stream)
-    torch.cuda.synchronize()
-    t_wall1 = time.time()
-    barrier()
-    sampler.mark(t_wall0, t_wall1)
-    local_ms = start.elapsed_time(end)
-    sampled = [e for e in events if e is not None]
-    plan_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in sampled)
-    disp_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in sampled) / (1 + w.cached_steps)
-    comb_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in sampled)
-    agg = aggregate(led["total"], w.T, local_ms, world, args.steps)
+    b = Bench(ep, WORKLOADS[args.workload], dev, stream)
+    w, led, n_recv = b.w, b.led, b.n_recv
+    r = b.timed(args.steps, args.warmup, sampler, graph=args.launch == "graph")
+    agg = aggregate(led["total"], w.T, r["local_ms"], world, args.steps)
+    phases = phase_stats(r["phases"])
+    roofline = b.roofline(r["phases"])
 
     # End to end through the public API with host buffers: every step copies
     # its inputs (x for each dispatch, topk_idx, topk_weights) from pinned host
@@ -434,42 +578,42 @@ def run_ours(args):
     # are double buffered and every reuse waits on the event of the step that
     # used it.
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    x_pin = [[bits_to_bf16_tensor(xn).pin_memory() for xn in x_nps] for _ in range(2)]
-    idx_pin = torch.from_numpy(idx_np).pin_memory()
-    w_pin = torch.from_numpy(w_np).pin_memory()
+    x_pin = [[bits_to_bf16_tensor(xn).pin_memory() for xn in b.x_nps] for _ in range(2)]
+    idx_pin = torch.from_numpy(b.idx_np).pin_memory()
+    w_pin = torch.from_numpy(b.w_np).pin_memory()
     out_pin = [torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    xss = [x_ts, [torch.empty_like(xt) for xt in x_ts]]
-    idxs = [idx_t, torch.empty_like(idx_t)]
-    wtss = [wts_t, torch.empty_like(wts_t)]
-    outs = [out, torch.empty_like(out)]
-    hs = [h, ep.plan(idx_t, w.P, w.E, w.A, stream=stream)]
+    xss = [b.x_ts, [torch.empty_like(xt) for xt in b.x_ts]]
+    idxs = [b.idx_t, torch.empty_like(b.idx_t)]
+    wtss = [b.wts_t, torch.empty_like(b.wts_t)]
+    outs = [b.out, torch.empty_like(b.out)]
+    hs = [b.h, ep.plan(b.idx_t, w.P, w.E, w.A, stream=stream)]
     s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
 
     def run_e2e(n):
-        ev_done = [None, None]    # compute on buffer b finished
-        ev_out = [None, None]     # output of buffer b copied back
+        ev_done = [None, None]    # compute on buffer i finished
+        ev_out = [None, None]     # output of buffer i copied back
         for i in range(n):
-            b = i & 1
+            j = i & 1
             with torch.cuda.stream(s_h2d):
-                if ev_done[b] is not None:
-                    s_h2d.wait_event(ev_done[b])
-                for dst, src in zip(xss[b], x_pin[b]):
+                if ev_done[j] is not None:
+                    s_h2d.wait_event(ev_done[j])
+                for dst, src in zip(xss[j], x_pin[j]):
                     dst.copy_(src, non_blocking=True)
-                idxs[b].copy_(idx_pin, non_blocking=True)
-                wtss[b].copy_(w_pin, non_blocking=True)
+                idxs[j].copy_(idx_pin, non_blocking=True)
+                wtss[j].copy_(w_pin, non_blocking=True)
                 ev_in = torch.cuda.Event()
                 ev_in.record(s_h2d)
             stream.wait_event(ev_in)
-            if ev_out[b] is not None:
-                stream.wait_event(ev_out[b])
-            step(hh=hs[b], xs=xss[b], idx=idxs[b], wts=wtss[b], o=outs[b])
-            ev_done[b] = torch.cuda.Event()
-            ev_done[b].record(stream)
+            if ev_out[j] is not None:
+                stream.wait_event(ev_out[j])
+            b.step(hh=hs[j], xs=xss[j], idx=idxs[j], wts=wtss[j], o=outs[j])
+            ev_done[j] = torch.cuda.Event()
+            ev_done[j].record(stream)
             with torch.cuda.stream(s_d2h):
-                s_d2h.wait_event(ev_done[b])
-                out_pin[b].copy_(outs[b], non_blocking=True)
-                ev_out[b] = torch.cuda.Event()
-                ev_out[b].record(s_d2h)
+                s_d2h.wait_event(ev_done[j])
+                out_pin[j].copy_(outs[j], non_blocking=True)
+                ev_out[j] = torch.cuda.Event()
+                ev_out[j].record(s_d2h)
         return ev_out
 
     run_e2e(min(4, e2e_steps))
@@ -488,38 +632,54 @@ def run_ours(args):
     barrier()
     sampler.mark(t_wall0, t_wall1)
     agg_e2e = aggregate(led["total"], w.T, s2.elapsed_time(e2), world, e2e_steps)
-    clocks = sampler.stop()
     for hh in hs:
         status = hh.sync_status(stream)
         if status != ep.EP_OK:
             raise RuntimeError(f"device status {status} after the timed steps")
-        hh.destroy(stream)
+    hs[1].destroy(stream)
     h2d = sum(xp.numel() * 2 for xp in x_pin[0]) + idx_pin.numel() * 8 + w_pin.numel() * 4
     d2h = out_pin[0].numel() * 2
+    del x_pin, out_pin, xss, idxs, wtss, outs
 
-    # roofline of the dominant kernel
-    peak, peak_src = hbm_peak()
-    if disp_ms >= comb_ms:
-        kname = "ep_dispatch_fp8_kernel" if w.fp8 else "ep_dispatch_copy_kernel"
-        kfile, kbytes, kms = "ep_dispatch_kernels.cu", led["dispatch"], disp_ms
-    else:
-        kname, kfile, kbytes, kms = "ep_combine_kernel", "ep_combine_kernels.cu", led["combine"], comb_ms
-    achieved = kbytes / (kms / 1e3) / 1e9
-    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                else "fallback 6.8 TB/s", "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": profiled_traffic(kname, kfile, w.name), "algorithmic_bytes": kbytes}
+    overlap = run_overlap(ep, w, b.idx_t, b.x_ts[0], b.wts_t, stream, args) if args.overlap else None
+    cta_profile = run_cta_profile(ep, w, b.idx_t, b.x_ts[0], b.wts_t, b.y, stream, b.recv, b.recv_sc,
+                                  b.out_dtype) if args.cta_profile else None
+    b.close()
+    del b
+    torch.cuda.empty_cache()
+
+    # every other workload, device-timed: fewer steps each
+    workloads = {}
+    if not args.no_workloads:
+        wl_steps = max(4, min(args.steps, args.workload_steps))
+        wl_warm = max(3, min(args.warmup, 5))
+        for name in WORKLOADS:
+            if name == args.workload:
+                continue
+            bw = Bench(ep, WORKLOADS[name], dev, stream)
+            rw = bw.timed(wl_steps, wl_warm, sampler, graph=args.workload_launch == "graph")
+            if bw.h.sync_status(stream) != ep.EP_OK:
+                raise RuntimeError(f"device status after the {name} steps")
+            workloads[name] = workload_line(bw, rw, world, wl_steps)
+            bw.close()
+            del bw
+            torch.cuda.empty_cache()
+    clocks = sampler.stop()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        s = oracle_sample(w, min_seconds=8.0)
-        cpu = {"value": round(s["gbs"], 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"full {w.name} workload (T={w.T}, H={w.H}), {s['passes']} pass(es) of the step, "
-                         f"single-threaded C oracle", "tokens_per_s": round(s["tokens_per_s"], 1)}
-
-    overlap = run_overlap(ep, w, idx_t, x_t, wts_t, stream, args) if args.overlap else None
-    cta_profile = run_cta_profile(ep, w, idx_t, x_t, wts_t, y, stream, recv, recv_sc, out_dtype) \
-        if args.cta_profile else None
+        import oracle
+        single = oracle_sample(w, min_seconds=6.0, parallel=False)
+        multi = oracle_sample(w, min_seconds=6.0, parallel=True) if oracle.omp_available() else None
+        best = multi or single
+        cpu = {"value": round(best["gbs"], 4), "unit": "GB/s", "cores": best["threads"], "kind": "oracle",
+               "sample": f"full {w.name} workload (T={w.T}, H={w.H}), {best['passes']} pass(es) of the step, "
+                         + (f"OpenMP build of the C oracle on {best['threads']} threads (the scatter, "
+                            "expert and combine row loops split; the plan sequential)" if multi
+                            else "single-threaded C oracle"),
+               "tokens_per_s": round(best["tokens_per_s"], 1),
+               "single_thread": {"value": round(single["gbs"], 4), "unit": "GB/s", "cores": 1,
+                                 "passes": single["passes"], "tokens_per_s": round(single["tokens_per_s"], 1)}}
 
     if rank == 0:
         line = {
@@ -528,10 +688,12 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded Gumbel-top-k routing, N(0,1) bf16 hidden states)",
             "tokens_per_s": round(agg["tokens_per_s"], 1),
-            "hbm_roofline_frac": round(agg["gbs"] / world / peak, 4),
+            "hbm_roofline_frac": round(agg["gbs"] / world / hbm_peak()[0], 4),
             "config": workload_config(w),
-            "phases_ms": {"plan": round(plan_ms, 5), "dispatch": round(disp_ms, 5), "combine": round(comb_ms, 5),
-                          "sampled_steps": len(sampled)},
+            "launch": "one captured step replayed from a CUDA graph" if r["launch"] == "graph"
+            else "direct launches from the host",
+            "phases_ms": {**phases, "sampled_steps": r["sampled"],
+                          "stat": "median and max over the sampled steps"},
             "ledger_bytes_per_step": led,
             "payload_gbs": round(world * payload_ledger(w, n_recv) / (agg["ms_per_step"] / 1e3) / 1e9, 2),
             "roofline": roofline,
@@ -544,6 +706,7 @@ def run_ours(args):
             "gpu_launches": (2 + 1 + w.cached_steps) * args.steps,
             "clocks": clocks,
             "cpu_baseline": cpu,
+            "workloads": workloads,
         }
         if overlap is not None:
             line["overlap"] = overlap
@@ -551,6 +714,87 @@ def run_ours(args):
             line["cta_profile"] = cta_profile
         print(json.dumps(line), flush=True)
     barrier()
+    return 0
+
+
+def run_kernel_table(ep, args, local):
+    """Each kernel of the library alone, launched back to back on the
+    workload: plan, BF16 dispatch, quantising FP8 dispatch, dispatch of
+    pre-quantised FP8 input, dispatch metadata, combine, dispatch backward and
+    combine backward.  Per kernel: the average time of --steps launches
+    between two events (after --warmup untimed ones), its algorithmic bytes
+    and their rate against the measured copy bandwidth.  Prints one JSON line."""
+    import torch
+    from combine_ep_plan_gb300.inputs import WORKLOADS, bits_to_bf16_tensor, draw_hidden, draw_topk, hidden_seed
+    w = WORKLOADS[args.workload]
+    dev = torch.device("cuda", local)
+    st = torch.cuda.current_stream()
+    idx_np, w_np = draw_topk(w)
+    idx = torch.from_numpy(idx_np).to(dev)
+    wts = torch.from_numpy(w_np).to(dev)
+    x = bits_to_bf16_tensor(draw_hidden(w.T, w.H, hidden_seed(w))).to(dev)
+    h = ep.plan(idx, w.P, w.E, w.A, stream=st)
+    n_exp, n_recv = h.sizes(st)
+    cap = ep.worst_expanded_rows(w.T, w.K, w.E, w.A)
+    T, K, H = w.T, w.K, w.H
+    n_valid = int((idx >= 0).sum().item())
+    n_pad = n_exp - n_valid
+    G = H // 128
+    # pre-quantised input for the pass-through dispatch (scaffolding, not timed)
+    xs = (x.float().view(T, G, 128).abs().amax(dim=2) / 448.0).contiguous()
+    xq = (x.float().view(T, G, 128) / xs.clamp_min(1e-30)[:, :, None]).view(T, H).to(torch.float8_e4m3fn)
+    recv = torch.empty((cap, H), dtype=torch.bfloat16, device=dev)
+    recv8 = torch.empty((cap, H), dtype=torch.float8_e4m3fn, device=dev)
+    sc8 = torch.empty((cap, G), dtype=torch.float32, device=dev)
+    rw = torch.empty(cap, dtype=torch.float32, device=dev)
+    rm = torch.empty((cap, 2), dtype=torch.int32, device=dev)
+    out = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    gy = torch.empty((cap, H), dtype=torch.bfloat16, device=dev)
+    gw = torch.empty((T, K), dtype=torch.float32, device=dev)
+    ep.dispatch(h, x, "bf16", True, recv_x=recv, stream=st)
+    row8 = H + 4 * G
+    kernels = {
+        "ep_plan_kernel": (lambda: h.replan(idx, stream=st), step_ledger(w, n_exp, n_valid, n_recv)["plan"]),
+        "ep_dispatch_copy_kernel (bf16)": (
+            lambda: ep.dispatch(h, x, "bf16", True, recv_x=recv, stream=st), T * H * 2 + n_exp * H * 2 + T * K * 4),
+        "ep_dispatch_fp8_kernel": (
+            lambda: ep.dispatch(h, x, "fp8", True, recv_x=recv8, recv_scales=sc8, stream=st),
+            T * H * 2 + n_exp * row8 + T * K * 4),
+        "ep_dispatch_copy_kernel (fp8 input)": (
+            lambda: ep.dispatch(h, xq, "fp8", True, recv_x=recv8, recv_scales=sc8, stream=st, x_scales=xs),
+            T * row8 + n_exp * row8 + T * K * 4),
+        "ep_dispatch_metadata_kernel": (
+            lambda: ep.dispatch_metadata(h, wts, recv_weights=rw, recv_meta=rm, capacity=cap, stream=st),
+            T * K * 8 + n_exp * 12),
+        "ep_combine_kernel": (lambda: ep.combine(h, recv, wts, out=out, stream=st),
+                              n_valid * H * 2 + T * K * 8 + T * H * 2),
+        "ep_combine_kernel (dispatch backward)": (lambda: ep.dispatch_backward(h, recv, grad_x=out, stream=st),
+                                                  n_valid * H * 2 + T * K * 4 + T * H * 2),
+        "ep_combine_backward_kernel": (
+            lambda: ep.combine_backward(h, out, recv, wts, zero_pad=True, grad_y=gy, grad_weights=gw, stream=st),
+            T * H * 2 + 2 * n_valid * H * 2 + T * K * 12 + n_pad * H * 2),
+    }
+    peak, _ = hbm_peak()
+    res = {}
+    for name, (fn, nbytes) in kernels.items():
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        for _ in range(args.steps):
+            fn()
+        e.record(st)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(e) * 1e3 / args.steps
+        gbs = nbytes / (us * 1e-6) / 1e9
+        res[name] = {"us": round(us, 2), "bytes": int(nbytes), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)}
+    if h.sync_status(st) != ep.EP_OK:
+        raise RuntimeError("device status after the kernel table")
+    h.destroy(st)
+    print(json.dumps({"kernels": res, "workload": workload_config(w)["workload"], "launches_each": args.steps,
+                      "timing": "back-to-back launches between two CUDA events, after warm-up; "
+                                "bytes: algorithmic, per launch", "peak_gbs": peak}), flush=True)
     return 0
 
 
@@ -659,6 +903,17 @@ def main(argv=None):
     ap.add_argument("--workload", default="bf16")
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workloads (the `workloads` object of the line)")
+    ap.add_argument("--workload-steps", type=int, default=40,
+                    help="timed steps of each other workload (at most --steps)")
+    ap.add_argument("--launch", choices=["direct", "graph"], default="graph",
+                    help="timed steps of the headline workload: direct launches, or one captured step "
+                         "replayed from a CUDA graph")
+    ap.add_argument("--workload-launch", choices=["direct", "graph"], default="graph",
+                    help="the same for the other workloads")
+    ap.add_argument("--kernels", action="store_true",
+                    help="instead of the step: time each kernel of the library alone on the workload")
     ap.add_argument("--overlap", action="store_true",
                     help="also time dispatch issued on the communication stream under an SM budget, "
                          "overlapped with a shared-expert FFN on the compute stream")
