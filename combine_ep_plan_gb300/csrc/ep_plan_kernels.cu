@@ -783,6 +783,11 @@ int plan_grid(const PlanDev& p, int sm_budget) {
   int64_t grid = (work + EP_PLAN_WORK_PER_CTA - 1) / EP_PLAN_WORK_PER_CTA;
   if (grid < p.num_tiles) grid = p.num_tiles;
   if (grid > cap) grid = cap;
+  // the dense [T,P] pass keeps one rank per thread: at least P threads, even
+  // under a tight SM budget (the whole device co-hosts far more)
+  const int64_t min_grid = (p.P + kTile - 1) / kTile;
+  const int64_t full = static_cast<int64_t>(cached_per_sm) * num_sms();
+  if (grid < min_grid) grid = min_grid < full ? min_grid : full;
   return static_cast<int>(grid);
 }
 

@@ -94,6 +94,19 @@ def test_sm_budget_changes_no_result(w):
         h.destroy()
 
 
+def test_plan_under_a_one_sm_budget_with_more_ranks_than_its_threads():
+    """1024 ranks and a one-SM budget (two co-resident plan CTAs, 512
+    threads): the dense [T,P] pass keeps one rank per thread, so the plan
+    still takes enough CTAs for every rank."""
+    w = WORKLOADS["tiny"].scaled(P=1024, E=1024, S=1, K=2, A=2, H=256)
+    idx, _, _ = _inputs(w)
+    h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
+    h.set_num_sms(1)
+    h.replan(torch.from_numpy(idx).cuda())
+    assert h.sync_status() == ep.EP_OK
+    assert_plan_equal(gpu_plan_arrays(h), oracle.plan(idx, w.S, w.P, w.E, w.A))
+
+
 def test_sm_budget_rejects_negative():
     w = WORKLOADS["tiny"]
     idx, _, _ = _inputs(w)
