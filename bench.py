@@ -717,6 +717,29 @@ def run_ours(args):
     return 0
 
 
+def run_cpu_table(args):
+    """The CPU oracle on every workload, whole passes of the step: the
+    single-threaded build and the OpenMP build on all host threads.  Prints
+    one JSON line (rank 0 only)."""
+    import oracle
+    from combine_ep_plan_gb300.inputs import WORKLOADS
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return 0
+    res = {}
+    for name, w in WORKLOADS.items():
+        row = {}
+        for par in ([False, True] if oracle.omp_available() else [False]):
+            smp = oracle_sample(w, min_seconds=args.cpu_seconds, parallel=par)
+            row["omp" if par else "single"] = {"gbs": round(smp["gbs"], 4), "threads": smp["threads"],
+                                               "seconds_per_pass": round(smp["seconds_per_pass"], 3),
+                                               "passes": smp["passes"], "tokens_per_s": round(smp["tokens_per_s"], 1)}
+        res[name] = row
+    print(json.dumps({"cpu_table": res, "unit": "GB/s of the step's ledger",
+                      "timing": f"whole passes of the step until {args.cpu_seconds} s of CPU time"}), flush=True)
+    return 0
+
+
 def run_kernel_table(ep, args, local):
     """Each kernel of the library alone, launched back to back on the
     workload: plan, BF16 dispatch, quantising FP8 dispatch, dispatch of
@@ -912,6 +935,9 @@ def main(argv=None):
                          "replayed from a CUDA graph")
     ap.add_argument("--workload-launch", choices=["direct", "graph"], default="graph",
                     help="the same for the other workloads")
+    ap.add_argument("--cpu-table", action="store_true",
+                    help="instead of the step: the CPU oracle's rate on every workload (no GPU)")
+    ap.add_argument("--cpu-seconds", type=float, default=6.0)
     ap.add_argument("--kernels", action="store_true",
                     help="instead of the step: time each kernel of the library alone on the workload")
     ap.add_argument("--overlap", action="store_true",
@@ -923,6 +949,8 @@ def main(argv=None):
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, reported as used
     if args.impl == "reference":
         return run_reference(args)
+    if args.cpu_table:
+        return run_cpu_table(args)
     return run_ours(args)
 
 
