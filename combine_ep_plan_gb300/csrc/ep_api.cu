@@ -172,6 +172,7 @@ size_t layout_handle(ep_handle_s* h, char* base) {
   const size_t o_wpre = L.take(sizeof(int) * p.num_tiles * ep::kTileWords * (P + E));
   const size_t o_sizes = L.take(sizeof(int) * ep::kSizeWords);
   const size_t o_totals = L.take(sizeof(int) * (P + E));
+  const size_t o_trep = L.take(sizeof(int) * ep::kTotRep * (P + E));
   const size_t o_ntpe = L.take(sizeof(int) * P * E);
   // outputs
   const size_t o_ntpr = L.take(sizeof(int) * P * P);
@@ -200,6 +201,7 @@ size_t layout_handle(ep_handle_s* h, char* base) {
     p.tile_wpre = reinterpret_cast<int*>(base + o_wpre);
     p.sizes = reinterpret_cast<int*>(base + o_sizes);
     p.totals = reinterpret_cast<int*>(base + o_totals);
+    p.totals_rep = reinterpret_cast<int*>(base + o_trep);
     p.ntpe = reinterpret_cast<int*>(base + o_ntpe);
     p.agg = reinterpret_cast<int*>(base + o_agg);
     p.tile_pre = reinterpret_cast<int*>(base + o_tpre);

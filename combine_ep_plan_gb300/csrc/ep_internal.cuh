@@ -36,6 +36,12 @@ constexpr int kCtrBarGen = 64;    // generation
 constexpr int kCtrStatus = 96;    // device status word
 constexpr int kCtrWords = 128;
 
+// Copies of the column totals: every CTA reads the totals right after the
+// second grid barrier; spreading the reads over 16 copies (CTA b reads copy
+// b % 16) keeps them from queuing on the same few L2 lines (fp8 plan, 256
+// experts: 17.7 -> 16.5 us).
+constexpr int kTotRep = 16;
+
 // Size slots.
 constexpr int kSizeRecv = 0;  // N_recv
 constexpr int kSizeExp = 1;   // N_exp
@@ -179,6 +185,7 @@ struct PlanDev {
   // outputs
   int* sizes;          // [kSizeWords]
   int* totals;         // [P+E]: num_recv[d], then expert_counts[e]
+  int* totals_rep;     // [kTotRep][P+E]: copies of the totals, read by the CTAs in turn
   int* ntpe;           // [P,E]  num_tokens_per_expert
   int* ntpr;           // [P,P]
   int* rpm;            // [P,P]

@@ -169,6 +169,7 @@ __device__ void column_scans(const PlanDev& p) {
       }
     }
     if (lane == 0) p.totals[col] = carry;
+    if (lane < kTotRep) p.totals_rep[static_cast<int64_t>(lane) * p.ncols + col] = carry;
   }
 }
 
@@ -183,7 +184,7 @@ __device__ __forceinline__ int tile_pos(const uint32_t* bits, const int* s_run, 
 
 // X_col(g): bits set in column col for tokens before g (g in [0, T]).
 __device__ __forceinline__ int x_at(const PlanDev& p, int col, int64_t g) {
-  if (g >= p.T) return __ldcg(&p.totals[col]);
+  if (g >= p.T) return __ldcg(&p.totals_rep[static_cast<int64_t>(blockIdx.x % kTotRep) * p.ncols + col]);
   const int64_t t = g / kTile;
   const int gl = static_cast<int>(g - t * kTile);
   const int64_t at = (t * kTileWords + (gl >> 5)) * p.ncols + col;
@@ -371,7 +372,8 @@ __global__ void __launch_bounds__(kTile, kPlanThreadsPerSm / kTile) ep_plan_kern
   const bool own_tile = gridDim.x >= static_cast<unsigned>(p.num_tiles);
   const bool has_tile = own_tile && blockIdx.x < static_cast<unsigned>(p.num_tiles);
   if (threadIdx.x < 32) {
-    offsets_warp_scan<false>(p, p.totals, exp_off, pad_off, recv_off, s_sizes);
+    offsets_warp_scan<false>(p, p.totals_rep + static_cast<int64_t>(blockIdx.x % kTotRep) * p.ncols, exp_off, pad_off,
+                             recv_off, s_sizes);
   } else if (has_tile) {
     // the own tile's exclusive prefix per column
     for (int col = threadIdx.x - 32; col < p.ncols; col += blockDim.x - 32)

@@ -103,7 +103,8 @@ extern "C" ep_status_t ep_plan_static_scratch(const int64_t* topk_idx, int64_t S
   const size_t o_wpre = round256(o_bits + sizeof(uint32_t) * tile_words);
   const size_t o_sizes = round256(o_wpre + sizeof(int) * tile_words);
   const size_t o_totals = round256(o_sizes + sizeof(int) * ep::kSizeWords);
-  const size_t o_padoff = round256(o_totals + sizeof(int) * ncols);
+  const size_t o_trep = round256(o_totals + sizeof(int) * ncols);
+  const size_t o_padoff = round256(o_trep + sizeof(int) * ep::kTotRep * ncols);
   if (o_padoff + sizeof(int) * (E + 1) > EP_STATIC_SCRATCH_BYTES) return EP_ERR_CAPACITY;
 
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
@@ -137,6 +138,7 @@ extern "C" ep_status_t ep_plan_static_scratch(const int64_t* topk_idx, int64_t S
   p.tile_wpre = reinterpret_cast<int*>(base + o_wpre);
   p.sizes = reinterpret_cast<int*>(base + o_sizes);
   p.totals = reinterpret_cast<int*>(base + o_totals);
+  p.totals_rep = reinterpret_cast<int*>(base + o_trep);
   p.ntpe = out->num_tokens_per_expert;
   p.ntpr = out->num_tokens_per_rank;
   p.rpm = out->rank_prefix;

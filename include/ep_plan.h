@@ -362,8 +362,9 @@ ep_status_t ep_handle_destroy(ep_handle_t handle, ep_stream_t stream);
  *   call's contents; each call clears what it needs.  Calls whose work
  *   overlaps on the GPU (other streams, other threads) race on the scratch:
  *   order them.
- * - Scratch need: about 0.28*T*(P+E) + 4*(P+2E) + 2 KB bytes (per-tile
- *   counts and prefixes, tile bit matrices and their word prefixes); a plan that
+ * - Scratch need: about 0.28*T*(P+E) + 4*(17P+18E) + 2 KB bytes (per-tile
+ *   counts and prefixes, tile bit matrices and their word prefixes, column
+ *   totals and their copies); a plan that
  *   would need more than EP_STATIC_SCRATCH_BYTES returns EP_ERR_CAPACITY
  *   before anything is enqueued (16384 tokens with P+E = 384 need about
  *   1.8 MB; 65536 tokens fit with P+E up to about 220).
