@@ -235,6 +235,72 @@ def test_brute_force_tiny():
     assert pl.num_expanded == row
 
 
+def _brute_plan(idx, S, P, E, A, C):
+    """Every plan array from the definitions, with Python sets, lists and loops."""
+    T, K = idx.shape
+    El = E // P
+    chunk = -(-S // C)
+    dests = [sorted({int(e) // El for e in idx[g] if e >= 0}) for g in range(T)]
+    in_rank = np.array([[1 if d in dests[g] else 0 for d in range(P)] for g in range(T)], np.uint8)
+    ntpr = np.array([[sum(in_rank[s * S + t, d] for t in range(S)) for d in range(P)] for s in range(P)], np.int32)
+    ntpe = np.array([[sum(int(idx[s * S + t, k] == e) for t in range(S) for k in range(K)) for e in range(E)]
+                     for s in range(P)], np.int32)
+    rpm = np.array([[sum(ntpr[s2, d] for s2 in range(s + 1)) for d in range(P)] for s in range(P)], np.int32)
+    cpm = np.zeros((P, P, C), np.int32)
+    for s in range(P):
+        for d in range(P):
+            for c in range(C):
+                cpm[s, d, c] = sum(in_rank[s * S + t, d] for t in range(min(S, (c + 1) * chunk)))
+    rcpm = np.zeros((P, P, C), np.int32)
+    for d in range(P):
+        for s in range(P):
+            for c in range(C):
+                rcpm[d, s, c] = (rpm[s - 1, d] if s > 0 else 0) + (cpm[s, d, c - 1] if c > 0 else 0)
+    windows = [[g for g in range(T) if d in dests[g]] for d in range(P)]
+    send_head = -np.ones((T, P), np.int32)
+    recv_src = []
+    for d in range(P):
+        for pos, g in enumerate(windows[d]):
+            send_head[g, d] = pos
+            recv_src.append(g % S)
+    slot = -np.ones((T, K), np.int32)
+    exp_src, offsets = [], [0]
+    for e in range(E):
+        members = [(g, k) for g in range(T) for k in range(K) if idx[g, k] == e]
+        for g, k in members:
+            slot[g, k] = len(exp_src)
+            exp_src.append(g)
+        exp_src += [-1] * (-(-len(members) // A) * A - len(members))
+        offsets.append(len(exp_src))
+    return dict(is_token_in_rank=in_rank, num_tokens_per_rank=ntpr, num_tokens_per_expert=ntpe,
+                expert_counts=ntpe.sum(axis=0).astype(np.int32), num_recv=in_rank.sum(axis=0).astype(np.int32),
+                rank_prefix=rpm, channel_prefix=cpm, recv_channel_prefix=rcpm, send_head=send_head,
+                recv_offsets=np.concatenate([[0], np.cumsum([len(wd) for wd in windows])]).astype(np.int32),
+                recv_src_idx=np.array(recv_src, np.int32), expert_offsets=np.array(offsets, np.int32),
+                slot=slot, exp_src=np.array(exp_src, np.int32))
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_brute_force_random_shapes(i):
+    """Every plan array of the oracle against the Python brute force, on
+    random small shapes with unused slots, any channel count and padding."""
+    rng = np.random.default_rng(500 + i)
+    P = int(rng.integers(1, 7))
+    E = P * int(rng.integers(1, 5))
+    K = int(rng.integers(1, min(E, 5) + 1))
+    S = int(rng.integers(1, 41))
+    A = int(rng.choice([1, 2, 3, 8]))
+    C = int(rng.integers(1, S + 1))
+    w = WORKLOADS["tiny"].scaled(P=P, E=E, K=K, S=S, A=A, routing="zipf" if i % 3 == 0 else "uniform", seed=i)
+    idx, _ = draw_topk(w)
+    idx[rng.random(idx.shape) < 0.2] = -1
+    pl = oracle.plan(idx, S, P, E, A, C)
+    want = _brute_plan(idx, S, P, E, A, C)
+    for name, arr in want.items():
+        got = getattr(pl, name)
+        assert got.shape == arr.shape and np.array_equal(got, arr), name
+
+
 def test_single_rank_is_all_local():
     w = WORKLOADS["tiny"].scaled(P=1, S=128)
     idx, pl = _plan(w)
