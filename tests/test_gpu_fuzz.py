@@ -22,7 +22,7 @@ from ep_testutil import assert_bits_equal, assert_plan_equal, gpu_plan_arrays
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 40
+N_CASES = 100
 
 
 @pytest.fixture(scope="module", autouse=True)
