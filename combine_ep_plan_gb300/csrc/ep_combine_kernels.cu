@@ -188,6 +188,7 @@ __device__ __forceinline__ void combine_backward_item(const CombineBwdDev& c, in
   __shared__ float s_dot[kWarps][KMAX];
   const int64_t hv = c.H / 8;
   uint4* gy = static_cast<uint4*>(c.grad_y);
+  const unsigned long long pol = l2_evict_first_policy();  // the grad_y rows
   if (item >= c.T) {
     const int64_t pi = item - c.T;
     if (pi >= c.sizes[kSizePad] || pi >= c.max_pad) return;
@@ -197,7 +198,7 @@ __device__ __forceinline__ void combine_backward_item(const CombineBwdDev& c, in
       return;
     }
     for (int64_t v = threadIdx.x; v < hv; v += blockDim.x)
-      gy[static_cast<int64_t>(r) * hv + v] = make_uint4(0u, 0u, 0u, 0u);
+      st_evict_first(gy + static_cast<int64_t>(r) * hv + v, make_uint4(0u, 0u, 0u, 0u), pol);
     return;
   }
   const int64_t g = item;
@@ -254,7 +255,7 @@ __device__ __forceinline__ void combine_backward_item(const CombineBwdDev& c, in
       o.y = pack_bf16x2(__fmul_rn(wk[k], gof[2]), __fmul_rn(wk[k], gof[3]));
       o.z = pack_bf16x2(__fmul_rn(wk[k], gof[4]), __fmul_rn(wk[k], gof[5]));
       o.w = pack_bf16x2(__fmul_rn(wk[k], gof[6]), __fmul_rn(wk[k], gof[7]));
-      gy[static_cast<int64_t>(row[k]) * hv + v] = o;
+      st_evict_first(gy + static_cast<int64_t>(row[k]) * hv + v, o, pol);
     }
   }
   const int lane = threadIdx.x & 31;

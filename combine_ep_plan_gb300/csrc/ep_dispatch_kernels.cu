@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
   const int64_t n_items = (a.T + n_pad) * chunks;
   const uint4* x = static_cast<const uint4*>(a.x);
   uint4* out = static_cast<uint4*>(a.out);
+  const unsigned long long pol = l2_evict_first_policy();  // the written rows
 
   for (int64_t item = warp; item < n_items; item += nwarps) {
     const int64_t ri = item / chunks;
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
           const int64_t v = v0 + u * 32 + lane;
-          if (v < hv) st_row(dst + v, buf[u]);
+          if (v < hv) st_evict_first(dst + v, buf[u], pol);
         }
         if (copy_scales)
           for (int64_t j = lane; j < groups; j += 32) a.scales[scale_at(a, r, j, groups)] = a.x_scales[g * groups + j];
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(256) ep_dispatch_copy_kernel(DispatchDev a) {
 #pragma unroll
       for (int u = 0; u < kUnroll; ++u) {
         const int64_t v = v0 + u * 32 + lane;
-        if (v < hv) st_row(dst + v, z);
+        if (v < hv) st_evict_first(dst + v, z, pol);
       }
       if (WITH_SCALES && v0 == 0)
         for (int64_t j = lane; j < groups; j += 32) a.scales[scale_at(a, r, j, groups)] = 0.0f;
