@@ -335,7 +335,7 @@ def workload_config(w, sample_S=None) -> dict:
          "ranks": w.P, "experts": w.E, "tokens": w.T, "hidden": w.H, "topk": w.K, "expert_alignment": w.A,
          "l2": "no flush: inputs larger than L2 (x %.0f MB, expanded rows ~%.2f GB per step)" % (
              w.T * w.H * 2 / 1e6, w.T * w.K * w.H * 2 / 1e9)}
-    if sample_S is not None:
+    if sample_S is not None and sample_S != w.S:  # a sample smaller than the workload
         c["sample_tokens_per_rank"] = sample_S
     return c
 

@@ -110,3 +110,11 @@ def test_profile_summaries_name_their_command():
         assert cmds, n
         for line in cmds:
             assert "_work/" not in line and "python bench.py" in line, (n, line)
+
+
+def test_reference_config_names_a_sample_only_when_it_is_smaller():
+    """The reference arm's config equals the measured arm's when its sample
+    is the whole workload, and names the sample size only when it is not."""
+    w = WORKLOADS["bf16"]
+    assert bench.workload_config(w, sample_S=w.S) == bench.workload_config(w)
+    assert bench.workload_config(w, sample_S=w.S // 4)["sample_tokens_per_rank"] == w.S // 4
