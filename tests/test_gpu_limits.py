@@ -65,3 +65,25 @@ def test_bf16_small_and_ragged_hidden(H):
 
 def test_one_token_per_rank():
     _round_trip(WORKLOADS["rt"].scaled(S=1, H=256))
+
+
+@pytest.mark.parametrize("H", [128, 4224, 16384, 16512])
+def test_fp8_input_scale_group_counts(H):
+    """Pre-quantised input with 1, 33, 128 and 129 scale groups per row: the
+    scales of a row are held in registers up to 128 groups, beyond that the
+    rest is read again per destination; row- and column-major scales."""
+    w = WORKLOADS["fp8"].scaled(S=6, H=H)
+    idx, _ = draw_topk(w)
+    pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
+    h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
+    rng = np.random.default_rng(H)
+    xq = rng.integers(0, 256, size=(w.T, H), dtype=np.uint8)
+    xq[(xq & 0x7F) == 0x7F] = 0  # no NaN codes in the input
+    xs = rng.standard_normal((w.T, H // 128)).astype(np.float32)
+    q_ref, s_ref = oracle.dispatch_fp8_input(xq, xs, pl)
+    xq_t = torch.from_numpy(xq).cuda().view(torch.float8_e4m3fn)
+    for col_major in (False, True):
+        recv, sc = ep.dispatch(h, xq_t, "fp8", True, x_scales=torch.from_numpy(xs).cuda(), scales_col_major=col_major)
+        assert h.sync_status() == ep.EP_OK
+        assert np.array_equal(u8(recv), q_ref)
+        assert np.array_equal(sc.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
