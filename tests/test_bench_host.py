@@ -100,9 +100,9 @@ def test_reference_arm_prints_one_line_on_cpu():
 
 def test_profile_summaries_name_their_command():
     """Every committed ncu summary states the command that made it, and that
-    command runs committed files only."""
+    command runs committed files only (README.md is the index)."""
     prof = os.path.join(ROOT, "profiles")
-    names = [n for n in os.listdir(prof) if n.endswith(".md")]
+    names = [n for n in os.listdir(prof) if n.endswith(".md") and n != "README.md"]
     assert names
     for n in names:
         text = open(os.path.join(prof, n)).read()
