@@ -115,6 +115,19 @@ def step_ledger(w, n_exp: int, n_valid: int, n_recv: int) -> dict:
     return led
 
 
+# The source pages' own throughput figures, reported beside ours as context
+# only: per-rank bus bandwidth of an interconnect-bound Ascend supernode, FP8
+# dispatch and BF16 combine at hidden 7168, top-6, 256 experts; not a target
+# for, and not comparable with, one GPU's HBM traffic.
+PAGES_CONTEXT = {
+    "hardware": "Ascend 950DT 128-card supernode, per-rank bus bandwidth over its interconnect",
+    "dispatch_fp8_gbs_per_rank": {"EP8": "373-375", "EP16": "348-352", "EP32": "335-340", "EP128": "313"},
+    "combine_bf16_gbs_per_rank": {"EP8": "345-347", "EP128": "272"},
+    "dispatch_efficiency": "90-95 % of the physical payload bandwidth limit, EP up to 32",
+    "comparable_here": "payload_gbs (received token rows times per-token bytes, no padding)",
+}
+
+
 def payload_ledger(w, n_recv: int) -> int:
     """The pages' 'physical payload' form: received (token, destination) rows
     times the per-token bytes of x, topk_idx and topk_weights, no padding."""
@@ -696,6 +709,7 @@ def run_ours(args):
                           "stat": "median and max over the sampled steps"},
             "ledger_bytes_per_step": led,
             "payload_gbs": round(world * payload_ledger(w, n_recv) / (agg["ms_per_step"] / 1e3) / 1e9, 2),
+            "pages_context": PAGES_CONTEXT,
             "roofline": roofline,
             "e2e": {"value": round(agg_e2e["gbs"], 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(agg_e2e["ms_per_step"], 4),
