@@ -87,3 +87,23 @@ def test_fp8_input_scale_group_counts(H):
         assert h.sync_status() == ep.EP_OK
         assert np.array_equal(u8(recv), q_ref)
         assert np.array_equal(sc.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+
+
+def test_a_million_tokens():
+    """2^20 tokens (8 ranks x 131072, 4096 tiles, about 6.3 M expanded rows):
+    every plan array, the BF16 dispatch and the combine at H = 8, against the
+    oracle, whole arrays."""
+    w = WORKLOADS["bf16"].scaled(S=131072, H=8)
+    idx, wts = draw_topk(w)
+    idx[::9, 2] = -1
+    with oracle.parallel():
+        pl = oracle.plan(idx, w.S, w.P, w.E, w.A)
+        h = ep.plan(torch.from_numpy(idx).cuda(), w.P, w.E, w.A)
+        assert_plan_equal(gpu_plan_arrays(h), pl)
+        x = draw_hidden(w.T, w.H, hidden_seed(w))
+        recv, _ = ep.dispatch(h, bits_to_bf16_tensor(x).cuda(), "bf16", True)
+        ref = oracle.dispatch_bf16(x, pl, True)
+        assert np.array_equal(u16(recv), ref)
+        out = ep.combine(h, recv, torch.from_numpy(wts).cuda())
+        assert np.array_equal(u16(out), oracle.combine(ref, pl, wts))
+    assert h.sync_status() == ep.EP_OK
