@@ -125,7 +125,9 @@ const char *ep_status_string(ep_status_t status);
  * topk_idx_dev        [T,K] int64, row-major, 8-byte aligned.  Entry -1 marks
  *                     an unused slot; other entries must be distinct experts
  *                     in [0,E) (device-checked, EP_ERR_INVALID on sync).
- *                     Read during the call only; the handle keeps no reference.
+ *                     Read by the plan's kernel on `stream`: keep it unchanged
+ *                     until the stream has passed the plan.  The handle keeps
+ *                     no reference to it (later calls use the plan arrays).
  * num_tokens_per_rank S >= 1; T = P*S.
  * num_ranks           P, 1..EP_MAX_RANKS, E % P == 0.
  * num_topk            K, 1..min(E, EP_MAX_TOPK).
