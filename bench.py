@@ -233,9 +233,9 @@ def profiled_traffic(kernel: str, kernel_file: str, workload: str):
             vals[k.strip()] = quoted.group(1) if quoted else v.strip()
     if vals.get("source_sha256") != source_digest(kernel_file):
         return None
-    try:
-        return float(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
+    try:  # the number, before any note in parentheses
+        return float(vals["dram_bytes_per_launch"].split()[0])
+    except (KeyError, ValueError, IndexError):
         return None
 
 
@@ -290,8 +290,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    from combine_ep_plan_gb300.inputs import WORKLOADS, draw_hidden, draw_topk, hidden_seed
-    full = WORKLOADS[args.workload]
+    from combine_ep_plan_gb300.inputs import draw_hidden, draw_topk, hidden_seed
+    full = pick_workload(args)
     parallel = oracle.omp_available()
     with oracle.parallel(parallel):
         threads = oracle.threads()
@@ -330,6 +330,15 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def pick_workload(args):
+    """The workload of --workload, with --tokens-per-rank tokens per rank if given."""
+    from combine_ep_plan_gb300.inputs import WORKLOADS
+    w = WORKLOADS[args.workload]
+    if args.tokens_per_rank:
+        w = w.scaled(S=args.tokens_per_rank, name=f"{w.name}_S{args.tokens_per_rank}")
+    return w
 
 
 def step_description(w) -> str:
@@ -575,7 +584,7 @@ def run_ours(args):
     sampler = ClockSampler(local)
     sampler.start()
 
-    b = Bench(ep, WORKLOADS[args.workload], dev, stream)
+    b = Bench(ep, pick_workload(args), dev, stream)
     w, led, n_recv = b.w, b.led, b.n_recv
     r = b.timed(args.steps, args.warmup, sampler, graph=args.launch == "graph")
     agg = aggregate(led["total"], w.T, r["local_ms"], world, args.steps)
@@ -762,8 +771,8 @@ def run_kernel_table(ep, args, local):
     between two events (after --warmup untimed ones), its algorithmic bytes
     and their rate against the measured copy bandwidth.  Prints one JSON line."""
     import torch
-    from combine_ep_plan_gb300.inputs import WORKLOADS, bits_to_bf16_tensor, draw_hidden, draw_topk, hidden_seed
-    w = WORKLOADS[args.workload]
+    from combine_ep_plan_gb300.inputs import bits_to_bf16_tensor, draw_hidden, draw_topk, hidden_seed
+    w = pick_workload(args)
     dev = torch.device("cuda", local)
     st = torch.cuda.current_stream()
     idx_np, w_np = draw_topk(w)
@@ -959,6 +968,10 @@ def main(argv=None):
                          "overlapped with a shared-expert FFN on the compute stream")
     ap.add_argument("--cta-profile", action="store_true",
                     help="also run one step with per-CTA profile records and summarise them")
+    ap.add_argument("--tokens-per-rank", type=int, default=0,
+                    help="run the workload with this many tokens per rank instead of its own (a smaller "
+                         "case of the same kernels, e.g. for a profiler capture); it is then named "
+                         "<workload>_S<n>")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)  # at least 3 untimed warm-up steps, reported as used
     if args.impl == "reference":

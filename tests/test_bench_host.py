@@ -77,6 +77,8 @@ def test_profiled_traffic_requires_matching_source_hash(tmp_path, monkeypatch):
     (prof / "k.bf16.md").write_text(f"# x\n- source_sha256: `{digest}` (sha256 prefix when captured)\n"
                                     "- dram_bytes_per_launch: 123.5\n")
     (prof / "k2.bf16.md").write_text("- source_sha256: `deadbeef`\n- dram_bytes_per_launch: 9\n")
+    (prof / "k3.rt.md").write_text(f"- source_sha256: `{digest}`\n- dram_bytes_per_launch_captured: 7 (small)\n"
+                                   "- dram_bytes_per_launch: 28 (scaled to a full launch)\n")
     real_root = bench.ROOT
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     os.makedirs(tmp_path / "combine_ep_plan_gb300" / "csrc")
@@ -85,6 +87,7 @@ def test_profiled_traffic_requires_matching_source_hash(tmp_path, monkeypatch):
     assert bench.profiled_traffic("k", "ep_dispatch_kernels.cu", "bf16") == 123.5
     assert bench.profiled_traffic("k2", "ep_dispatch_kernels.cu", "bf16") is None
     assert bench.profiled_traffic("missing", "ep_dispatch_kernels.cu", "bf16") is None
+    assert bench.profiled_traffic("k3", "ep_dispatch_kernels.cu", "rt") == 28.0  # a scaled capture's note
 
 
 def test_reference_arm_prints_one_line_on_cpu():
